@@ -1,0 +1,524 @@
+#!/usr/bin/env python3
+"""Throughput of the grouped MoE low-precision hot path on GB300.
+
+One step = one NVFP4 mixture-of-experts up-projection over a batch of
+synthetic tokens already resident in HBM:
+    padded scale offsets -> per-expert amax -> NVFP4 tensor scales ->
+    grouped NVFP4 activation quantize -> fused grouped NVFP4 GEMM + SwiGLU +
+    NVFP4 requant
+on 128 experts, 16384 tokens routed top-8 uniformly (131072 rows), hidden
+K = 4096, I = 1536 (N = 2 x 1536 gate/up interleaved).  ``value`` is GEMM
+TFLOP/s of the whole step (2 * rows * N * K per step).  The line also carries
+the per-kernel figures of the other workloads (grouped quantize GB/s, FP8
+rowwise TFLOP/s, decode-shaped GB/s, the chained GEMM -> SwiGLU path), the
+dominant kernel's roofline, the sampled SM clocks, an end-to-end figure
+through the same calls from pinned host buffers, and the CPU oracle timed on
+a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+For N > 1 launch with torch.distributed.run: every rank runs the same step on
+its own batch (weak scaling, no collective on the data path); the time is the
+maximum over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped MoE GEMM TFLOPS (FP8/NVFP4) % of peak; quantize GB/s % of HBM"
+WORKLOAD = ("NVFP4 MoE up-projection: 128 experts, 16384 tokens top-8 uniform -> 131072 rows, "
+            "K=4096, N=2x1536 gate/up interleaved; amax -> NVFP4 quantize -> fused "
+            "GEMM+SwiGLU+NVFP4 requant")
+E4, TOK4, TOPK4, K4, I4 = 128, 16384, 8, 4096, 1536
+FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratios
+FP8_OVER_BF16 = 4.5 / 2.25
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
+    p.add_argument("--no-parts", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ setup
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampled every 100 ms while the GPU works."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+         "utilization.gpu")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "hw": f[5], "hwt": f[6],
+                             "swt": f[7], "pcap": f[8], "util": float(f[9])})
+            except ValueError:
+                continue
+        busy = [r for r in rows if r["util"] > 0] or rows
+        if not busy:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in busy):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in busy), "reasons": reasons,
+                "samples": len(busy)}
+
+
+# --------------------------------------------------------------- workload
+
+def up_projection_inputs(seed, device="cuda"):
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    counts = synth.routing_counts(TOK4, TOPK4, E4, seed=seed)
+    ro, ids = synth.ragged_groups(counts)
+    T = int(ro[-1])
+    rows = int(sum((int(c) + 127) // 128 * 128 for c in counts if c))
+    N = 2 * I4
+    d = {
+        "counts": counts, "ro_h": ro, "ids_h": ids, "T": T, "rows": rows, "N": N,
+        "ro": torch.from_numpy(ro.view(np.int32)).to(device),
+        "ids": torch.from_numpy(ids).to(device),
+        "so": torch.empty(len(ids) + 1, dtype=torch.int32, device=device),
+        "x": synth.bf16_normal((T, K4), 1.0, seed=seed + 1, device=device),
+        "b": synth.random_fp4_packed((E4, N, K4 // 2), seed=seed + 2, device=device),
+        "bsf": synth.random_bytes(E4 * moeq.sf_bytes(N, K4 // 16), 0x18, 0x28, seed=seed + 3,
+                                  device=device),
+        "es": synth.uniform((E4,), 0.5, 2.0, seed=seed + 4, device=device),
+        "ots": synth.uniform((E4,), 1.0, 4.0, seed=seed + 5, device=device),
+        "ts": torch.empty(E4, device=device),
+        "a": torch.empty((T, K4 // 2), dtype=torch.uint8, device=device),
+        "asf": torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8, device=device),
+        "c": torch.empty((T, I4 // 2), dtype=torch.uint8, device=device),
+        "csf": torch.empty(moeq.sf_bytes(rows, I4 // 16), dtype=torch.uint8, device=device),
+    }
+    d["mt"] = int(counts.max())
+    return d
+
+
+def up_projection_step(d, events=None):
+    """The hot path; `events` (list of 5 CUDA events) brackets each kernel."""
+    from fp4_fp8_quantization_gb300 import moeq
+    rec = (lambda i: events[i].record()) if events else (lambda i: None)
+    rec(0)
+    moeq.padded_scale_offsets(d["ro"], d["so"])
+    moeq.grouped_amax_scale(d["x"], d["ro"], d["ids"], d["ts"], E4)
+    rec(1)
+    moeq.grouped_quantize("nvfp4", d["x"], d["a"], d["asf"], d["ro"], d["so"], d["ids"], d["ts"],
+                          E4, d["rows"], d["mt"])
+    rec(2)
+    moeq.grouped_matmul_swiglu(d["c"], d["csf"], d["a"], d["asf"], d["b"], d["bsf"], d["es"],
+                               d["ots"], d["ro"], d["so"], d["ids"], I4, K4, d["rows"], d["mt"])
+    rec(3)
+
+
+KERNELS_PER_STEP = 5   # padded offsets, amax, amax finalize, quantize, fused GEMM
+
+
+def flops_up(d):
+    return 2.0 * d["T"] * d["N"] * K4
+
+
+# ------------------------------------------------------------ sub-parts
+
+def time_kernel(fn, iters, flush=None, warmup=3):
+    """Mean device time (ms) of fn(); an L2 flush (write of a buffer larger
+    than L2) precedes every timed call when `flush` is given."""
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+
+def parts(pk, flush):
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    hbm = pk["hbm_gbs"]
+    fp8_peak = pk["bf16"] * FP8_OVER_BF16
+    out = {}
+    dev = "cuda"
+    u32 = lambda a: torch.from_numpy(np.asarray(a, np.uint32).view(np.int32)).to(dev)
+
+    # grouped activation quantize: 8 experts, 4096 tokens top-2, hidden 4096
+    counts = synth.routing_counts(4096, 2, 8, seed=0)
+    ro, ids = synth.ragged_groups(counts)
+    T = int(ro[-1])
+    rows = int(sum((int(c) + 127) // 128 * 128 for c in counts if c))
+    x = synth.bf16_normal((T, 4096), 1.0, seed=1, device=dev, outlier_p=0.001, outlier_scale=50.0)
+    ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+    so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
+    moeq.padded_scale_offsets(ro_d, so_d)
+    ts = torch.empty(8, device=dev)
+    t_amax = time_kernel(lambda: moeq.grouped_amax_scale(x, ro_d, ids_d, ts, 8), 20, flush)
+    for fmt, ob, v in (("nvfp4", 2048, 16), ("mxfp8", 4096, 32)):
+        q = torch.empty((T, ob), dtype=torch.uint8, device=dev)
+        sf = torch.empty(moeq.sf_bytes(rows, 4096 // v), dtype=torch.uint8, device=dev)
+        ms = time_kernel(lambda: moeq.grouped_quantize(fmt, x, q, sf, ro_d, so_d, ids_d, ts, 8,
+                                                       rows), 20, flush)
+        nbytes = T * 4096 * 2 + q.numel() + sf.numel()
+        out[f"quantize_{fmt}_8192x4096"] = {
+            "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
+            "frac_hbm": round(nbytes / ms / 1e6 / hbm, 4), "bytes": nbytes}
+    out["amax_8192x4096"] = {"ms": round(t_amax, 5),
+                             "GB/s": round(T * 4096 * 2 / t_amax / 1e6, 1)}
+    del x
+
+    # FP8 rowwise at MoE scale: 64 experts, 8192 tokens top-8 Zipf(1.1), K 7168, N 4096
+    counts = synth.routing_counts(8192, 8, 64, seed=0, zipf_s=1.1)
+    ro, ids = synth.ragged_groups(counts)
+    T, N, K = int(ro[-1]), 4096, 7168
+    a, sa = synth.fp8_rowwise((T, K), 1.0, seed=10, device=dev)
+    b, sb = synth.fp8_rowwise((64, N, K), 0.02, seed=11, device=dev)
+    c = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+    ms = time_kernel(lambda: moeq.grouped_matmul_rowwise_fp8(
+        c, a, b, sa, sb.reshape(64, N), ro_d, ids_d, int(counts.max())), 10)
+    fl = 2.0 * T * N * K
+    out["fp8_rowwise_65536x4096x7168"] = {
+        "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
+        "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4)}
+    del a, b, c
+
+    # decode-shaped: 256 experts, 64 tokens top-8 -> 512 rows, K 7168, N 4096
+    counts = synth.routing_counts(64, 8, 256, seed=0)
+    ro, ids = synth.ragged_groups(counts)
+    T = int(ro[-1])
+    active_bytes = len(ids) * N * K
+    a, sa = synth.fp8_rowwise((T, K), 1.0, seed=20, device=dev)
+    b, sb = synth.fp8_rowwise((256, N, K), 0.02, seed=21, device=dev)
+    c = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+    ms = time_kernel(lambda: moeq.grouped_matmul_rowwise_fp8(
+        c, a, b, sa, sb.reshape(256, N), ro_d, ids_d, int(counts.max())), 10, flush)
+    out["decode_fp8_rowwise_512rows_224experts"] = {
+        "ms": round(ms, 4), "GB/s_active_weights": round(active_bytes / ms / 1e6, 1),
+        "frac_hbm": round(active_bytes / ms / 1e6 / hbm, 4), "active_experts": len(ids)}
+    del b
+    rows = int(sum((int(cc) + 127) // 128 * 128 for cc in counts if cc))
+    so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
+    moeq.padded_scale_offsets(ro_d, so_d)
+    b8 = synth.e4m3_normal((256, N, K), 1.0, seed=22, device=dev).view(torch.uint8)
+    bsf = synth.random_bytes(256 * moeq.sf_bytes(N, K // 32), 116, 126, seed=23, device=dev)
+    asf = synth.random_bytes(moeq.sf_bytes(rows, K // 32), 118, 130, seed=24, device=dev)
+    ms = time_kernel(lambda: moeq.grouped_matmul_blockscaled(
+        "mxfp8", c, a.view(torch.uint8), asf, b8, bsf, None, ro_d, so_d, ids_d, N, K, rows,
+        int(counts.max())), 10, flush)
+    wbytes = active_bytes + len(ids) * moeq.sf_bytes(N, K // 32)
+    out["decode_mxfp8_512rows_224experts"] = {
+        "ms": round(ms, 4), "GB/s_active_weights": round(wbytes / ms / 1e6, 1),
+        "frac_hbm": round(wbytes / ms / 1e6 / hbm, 4)}
+    del a, b8, c
+    return out
+
+
+def chained_part(d, pk):
+    from fp4_fp8_quantization_gb300 import moeq
+    y = torch.empty((d["T"], d["N"]), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty_like(d["c"])
+    csf = torch.empty_like(d["csf"])
+
+    def gemm():
+        moeq.grouped_matmul_blockscaled("nvfp4", y, d["a"], d["asf"], d["b"], d["bsf"], d["es"],
+                                        d["ro"], d["so"], d["ids"], d["N"], K4, d["rows"], d["mt"])
+
+    def sw():
+        moeq.swiglu_quantize(c, csf, y, d["ots"], d["ro"], d["so"], d["ids"], E4, d["rows"],
+                             d["mt"])
+
+    t_g = time_kernel(gemm, 10)
+    t_s = time_kernel(sw, 10)
+    same = bool(torch.equal(c, d["c"]) and torch.equal(csf, d["csf"]))
+    fl = flops_up(d)
+    return {"gemm_bf16_ms": round(t_g, 4), "gemm_TFLOP/s": round(fl / t_g / 1e9, 1),
+            "swiglu_quantize_ms": round(t_s, 4),
+            "swiglu_quantize_GB/s": round((y.numel() * 2 + c.numel() + csf.numel()) / t_s / 1e6, 1),
+            "chained_total_ms": round(t_g + t_s, 4), "fused_bytes_equal_chained": same}
+
+
+# --------------------------------------------------------- CPU baseline
+
+def cpu_oracle_sample(d, groups, max_rows=None):
+    """Times the CPU oracle on the chosen groups of the up-projection
+    workload (amax -> NVFP4 quantize -> float64 GEMM -> SwiGLU -> requant).
+    Returns (seconds, flops, rows)."""
+    from oracle import formats as F
+    from oracle import gemm as OG
+    from oracle import quantize as Q
+    from oracle import swiglu as S
+    ro, ids = d["ro_h"], d["ids_h"]
+    rows_list, eids = [], []
+    for g in groups:
+        r0, r1 = int(ro[g]), int(ro[g + 1])
+        if max_rows:
+            r1 = min(r1, r0 + max_rows)
+        rows_list.append((r0, r1))
+        eids.append(int(ids[g]))
+    counts = [r1 - r0 for r0, r1 in rows_list]
+    sro = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    sids = np.arange(len(groups), dtype=np.int32)
+    idx = np.concatenate([np.arange(r0, r1) for r0, r1 in rows_list])
+    x = d["x"][torch.from_numpy(idx).cuda()].float().cpu().numpy()
+    N = d["N"]
+    per = (N + 127) // 128 * (K4 // 64) * 512
+    eid_t = torch.tensor(eids, device="cuda")
+    b = d["b"][eid_t].cpu().numpy()
+    bsf = d["bsf"].view(E4, per)[eid_t].cpu().numpy().reshape(-1)
+    es = d["es"][eid_t].cpu().numpy()
+    ots = d["ots"][eid_t].cpu().numpy()
+    t0 = time.perf_counter()
+    so = Q.padded_scale_offsets(sro)
+    ts = Q.tensor_scale_from_amax(Q.group_amax(x, sro, sids, len(groups)))
+    qa, qsf = Q.grouped_quantize("nvfp4", x, sro, so, sids, ts)
+    ybits = OG.grouped_matmul_blockscaled("nvfp4", qa, qsf, b, bsf, es, sro, so, sids, N=N, K=K4,
+                                          scale_rows_total=int(so[-1]))
+    S.swiglu_quantize(F.decode_bf16(ybits), ots, sro, so, sids)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * len(idx) * N * K4, len(idx)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    d = up_projection_inputs(seed=0)
+    g = int(np.argmax(np.diff(d["ro_h"].astype(np.int64))))
+    rows_per_step = 256
+    for _ in range(args.warmup):
+        cpu_oracle_sample(d, [g], rows_per_step)
+    tot, fl = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, f, _ = cpu_oracle_sample(d, [g], rows_per_step)
+        tot += dt
+        fl += f
+    value = fl / tot / 1e12
+    sample = (f"{rows_per_step} rows of one expert group per step through the CPU oracle "
+              "(amax, NVFP4 quantize, float64 GEMM, SwiGLU, NVFP4 requant)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas{args.gpus}"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_moeq(args, rank, world):
+    from fp4_fp8_quantization_gb300 import moeq
+    moeq.lib()
+    pk = peaks()
+    d = up_projection_inputs(seed=1000 * rank)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        up_projection_step(d)
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(args.steps):
+        up_projection_step(d, evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    fl = flops_up(d)
+    value = world * fl / (ms_step * 1e-3) / 1e12
+
+    t_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_q = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_f = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    fp4_peak = pk["bf16"] * FP4_OVER_BF16
+    achieved = fl / (t_f * 1e-3) / 1e12
+    roof = {"kernel": "grouped_gemm_kernel<NVFP4, fused SwiGLU>", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / fp4_peak, 4), "traffic": None,
+            "peak_note": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio",
+            "algorithmic_flops_per_launch": fl}
+    breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
+                 "fused_gemm_swiglu_ms": round(t_f, 4)}
+
+    # end to end from pinned host buffers through the same calls
+    xh = d["x"].cpu().pin_memory()
+    roh = d["ro"].cpu().pin_memory()
+    idh = d["ids"].cpu().pin_memory()
+    ch = torch.empty(d["c"].shape, dtype=torch.uint8).pin_memory()
+    sfh = torch.empty(d["csf"].shape, dtype=torch.uint8).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        d["x"].copy_(xh, non_blocking=True)
+        d["ro"].copy_(roh, non_blocking=True)
+        d["ids"].copy_(idh, non_blocking=True)
+        up_projection_step(d)
+        ch.copy_(d["c"], non_blocking=True)
+        sfh.copy_(d["csf"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    h2d = xh.numel() * 2 + roh.numel() * 4 + idh.numel() * 4
+    d2h = ch.numel() + sfh.numel()
+    e2e = {"value": round(world * fl / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    extra = {}
+    if rank == 0 and not args.no_parts:
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+        extra["chained_same_workload"] = chained_part(d, pk)
+        extra.update(parts(pk, flush))
+        del flush
+    err = moeq.get_device_error()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        lens = np.diff(d["ro_h"].astype(np.int64))
+        groups = list(np.argsort(-lens)[:4])
+        dt, f, n = cpu_oracle_sample(d, groups)
+        cpu = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
+               "kind": "oracle", "seconds": round(dt, 2),
+               "sample": f"{n} rows (the 4 largest of 128 expert groups) through the CPU oracle: "
+                         "amax, NVFP4 quantize, float64 GEMM, SwiGLU, NVFP4 requant"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "experts": E4, "tokens": TOK4, "top_k": TOPK4,
+                       "rows": d["T"], "K": K4, "N": d["N"], "global_batch": world * TOK4,
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (1.07 GB bf16 activations, 0.81 GB FP4 weights)"},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk, "roofline": roof, "breakdown": breakdown, "e2e": e2e,
+            "cpu_baseline": cpu, "parts": extra, "device_error": err,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_moeq(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,409 @@
+// Device-side building blocks shared by the moeq kernels (sm_103a):
+// element codecs, the deterministic exp/SiLU, mbarrier / TMA / tcgen05
+// wrappers written as inline PTX, and bounded waits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moeq.h"
+
+namespace moeq {
+
+// ------------------------------------------------------------------ errors
+
+__device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// ------------------------------------------------------------------ codecs
+
+// bf16 bits -> fp32 (exact).
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return (uint32_t)__bfloat16_as_ushort(h);
+}
+
+// Eight fp32 -> eight E2M1 codes packed in 32 bits, element i in nibble i
+// (round to nearest even, saturating).  cvt.*x2 puts its first source in the
+// high half of the result, so each pair is given (x[2i+1], x[2i]).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8]) {
+    uint32_t r;
+    asm("{\n\t"
+        ".reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+        "}"
+        : "=r"(r)
+        : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]),
+          "f"(x[6]), "f"(x[7]));
+    return r;
+}
+
+// Two fp32 -> two E4M3 codes in 16 bits, lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+__device__ __forceinline__ uint32_t e4m3(float x) { return e4m3x2(x, 0.0f) & 0xFFu; }
+
+// Value of a non-negative finite E4M3 code (exact).
+__device__ __forceinline__ float e4m3_pos_value(uint32_t code) {
+    uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
+    if (e == 0) return (float)m * 0.001953125f;            // m * 2^-9
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// ------------------------------------------------------- NVFP4 block rule
+// One 16-element block: amax m, per-expert inverse tensor scale inv.
+// sb = E4M3((m * inv) / 6); r = inv / sb; codes = E2M1(x * r) (all +0 when
+// sb == 0).  Every step is one IEEE fp32 operation (no contraction).
+struct Nvfp4Scale {
+    uint32_t code;  // E4M3 scale code
+    float r;        // element multiplier, 0 when the block scale is 0
+};
+
+__device__ __forceinline__ Nvfp4Scale nvfp4_block_scale(float m, float inv) {
+    float sbf = __fdiv_rn(__fmul_rn(m, inv), 6.0f);
+    Nvfp4Scale s;
+    s.code = e4m3(sbf);
+    float sb = e4m3_pos_value(s.code);
+    s.r = (sb == 0.0f) ? 0.0f : __fdiv_rn(inv, sb);
+    return s;
+}
+
+// Eight elements of a block -> 32 bits of packed codes.
+__device__ __forceinline__ uint32_t nvfp4_codes8(const float (&x)[8], float r) {
+    if (r == 0.0f) return 0u;
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[i], r);
+    return e2m1x8(y);
+}
+
+// ------------------------------------------------ deterministic exp / SiLU
+// exp(x): Cody-Waite reduction x = n ln2 + f with ln 2 split into a
+// 16-significant-bit head (45426 / 2^16) and an fp32 tail, the degree-7
+// Taylor polynomial of e^f by Horner's rule with separately rounded
+// multiplies and adds, then two exact power-of-two multiplies by 2^(n/2).
+// x >= 89 gives +inf, x <= -104 gives 0.  The same steps are the library's
+// definition of the SwiGLU activation, so results are reproducible bit for bit.
+__device__ __forceinline__ float exp_spec(float x) {
+    const float kLog2e = 1.44269502162933349609375f;      // fp32(1 / ln 2)
+    const float kLn2Hi = 0.693145751953125f;              // 45426 / 65536
+    const float kLn2Lo = 1.428606765330187045037746429443359375e-06f;
+    const float c0 = 1.0f, c1 = 1.0f, c2 = 0.5f;
+    const float c3 = 0.16666667163372039794921875f;      // fp32(1/3!)
+    const float c4 = 0.0416666679084300994873046875f;    // fp32(1/4!)
+    const float c5 = 0.008333333767950534820556640625f;  // fp32(1/5!)
+    const float c6 = 0.001388888922519981861114501953125f;    // fp32(1/6!)
+    const float c7 = 0.0001984127011382952332496643066406f;   // fp32(1/7!)
+    if (x >= 89.0f) return __int_as_float(0x7f800000);
+    if (x <= -104.0f) return 0.0f;
+    float n = rintf(__fmul_rn(x, kLog2e));
+    float f = __fsub_rn(x, __fmul_rn(n, kLn2Hi));
+    f = __fsub_rn(f, __fmul_rn(n, kLn2Lo));
+    float p = c7;
+    p = __fadd_rn(__fmul_rn(p, f), c6);
+    p = __fadd_rn(__fmul_rn(p, f), c5);
+    p = __fadd_rn(__fmul_rn(p, f), c4);
+    p = __fadd_rn(__fmul_rn(p, f), c3);
+    p = __fadd_rn(__fmul_rn(p, f), c2);
+    p = __fadd_rn(__fmul_rn(p, f), c1);
+    p = __fadd_rn(__fmul_rn(p, f), c0);
+    int ni = (int)n;
+    int n1 = ni >> 1;                     // floor(n / 2)
+    int n2 = ni - n1;
+    float s1 = __int_as_float((n1 + 127) << 23);
+    float s2 = __int_as_float((n2 + 127) << 23);
+    return __fmul_rn(__fmul_rn(p, s1), s2);
+}
+
+__device__ __forceinline__ float silu_spec(float g) {
+    return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
+}
+
+// ----------------------------------------------------- tiled scale layout
+// Byte offset of the 4-byte word holding scale columns [4 kb, 4 kb + 4) of
+// logical row r, for kv_atoms = ceil(Kv / 4) atom columns.
+__device__ __forceinline__ int64_t sf_word_offset(int64_t r, int64_t kb, int64_t kv_atoms) {
+    return ((r >> 7) * kv_atoms + kb) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
+// ------------------------------------------------------------ group search
+// Largest g in [0, G) with offs[g] <= x (offs non-decreasing, offs[0] <= x).
+__device__ __forceinline__ int upper_bound_minus1(const uint32_t *offs, int G, uint32_t x) {
+    int lo = 0, hi = G;  // invariant: offs[lo] <= x, answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(offs + mid) <= x) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// ------------------------------------------------------------ PTX: memory
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// ~1 s at the GB300's maximum SM clock.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Waits for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) when *abort is set by another role, or after
+// kWaitLimitCycles, in which case it sets the timeout bit and *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint32_t *err) {
+    uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(a, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            set_error(err, MOEQ_DEVERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// TMA tiled loads into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// --------------------------------------------------------- PTX: tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrives on `bar` once every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand staged by TMA with 128B
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of one 512-byte scale atom in shared memory for tcgen05.cp
+// 32x128b: 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptors (dense, K-major A and B, fp32 accumulator).
+// kind::f8f6f4 with E4M3 x E4M3.
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// kind::mxf4nvf4, E2M1 x E2M1 with UE4M3 scales (16-element blocks).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// kind::mxf8f6f4, E4M3 x E4M3 with UE8M0 scales; sf_id picks the byte of
+// the 32-bit scale cell (the 32-element block within four).
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Copies one 512-byte scale atom (32 rows x 16 bytes) from shared memory to
+// 4 TMEM columns, replicated into all four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// --------------------------------------------------------- global stores
+
+__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+}  // namespace moeq

@@ -1,0 +1,550 @@
+// Grouped (ragged mixture-of-experts) GEMMs on the 5th-generation tensor
+// cores: FP8 rowwise-scaled, NVFP4 and MXFP8 block-scaled, with a bf16
+// epilogue or the fused SwiGLU + NVFP4 requantization epilogue.
+//
+// Pages: "grouped_matmul_rowwise_dynamic_scaled_fp8" (the rowwise formula,
+// fp32 accumulation, one post-reduction scale; its documented kernel is a
+// naive one with no persistent or TMA path), "max.nn.moe.NvMxf4f8Strategy"
+// (grouped_matmul: block-scaled with per-expert scales; grouped_matmul_swiglu:
+// GEMM + SwiGLU + quantize in one kernel, byte-identical to the chained path).
+//
+// Design (one CTA per SM, persistent):
+//  * tile scheduler: every CTA builds, in shared memory, the prefix over
+//    groups of ceil(rows_g / 128) * (N / BN) tiles from the device offsets,
+//    then walks tile ids blockIdx.x, blockIdx.x + gridDim.x, ...; a tile id
+//    maps to (group, m-block, n-block) by binary search on that prefix, with
+//    n fastest so that concurrently running CTAs share A rows and B[expert].
+//  * warp 0 (one thread): TMA producer.  A tiles (128 rows x 128 bytes of K)
+//    and B tiles (BN rows x 128 bytes) land 128B-swizzled in a STAGES-deep
+//    shared-memory ring; block-scaled kinds also bulk-copy the 512-byte
+//    scale atoms of the k-tile (contiguous in the tiled scale layout).
+//  * warp 1 (one thread): tcgen05.mma issuer.  Scale atoms go shared ->
+//    TMEM with tcgen05.cp (one TMEM slot per ring stage), the MMAs
+//    accumulate in one of two TMEM accumulators (double buffered, so the
+//    epilogue of tile i overlaps the mainloop of tile i+1), tcgen05.commit
+//    frees ring stages and publishes finished accumulators.
+//  * warps 2..5: epilogue.  Each warp owns a 32-lane quarter of TMEM (one
+//    row per thread), reads 32 fp32 columns at a time with tcgen05.ld and
+//    applies the scales (and SwiGLU + NVFP4 requant) in registers.
+//  * every wait is bounded (about one second) and sets the device error
+//    word instead of hanging.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moeq {
+
+namespace {
+
+enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2 };
+enum Epi { kBf16 = 0, kSwiglu = 1 };
+
+template <int KIND, int EPI, int BN_, int STAGES_>
+struct Cfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BK_BYTES = 128;                        // one 128B swizzle row
+    static constexpr int ELEMS_PER_BYTE = KIND == kNvfp4 ? 2 : 1;
+    static constexpr int BK = BK_BYTES * ELEMS_PER_BYTE;        // K elements per stage
+    static constexpr int KSTEPS = 4;                            // 32 bytes of K per MMA
+    static constexpr bool SCALED = KIND != kFp8Rowwise;
+    static constexpr int SF_VEC = KIND == kNvfp4 ? 16 : 32;
+    static constexpr int SF_ATOMS = SCALED ? BK / SF_VEC / 4 : 0;   // atoms per 128 rows per stage
+    static constexpr int SF_ATOM_BYTES = 512;
+    static constexpr int A_BYTES = BM * BK_BYTES;
+    static constexpr int B_BYTES = BN * BK_BYTES;
+    static constexpr int SFA_BYTES = SF_ATOMS * SF_ATOM_BYTES;
+    static constexpr int SFB_BYTES = SF_ATOMS * SF_ATOM_BYTES * (BN / 128);
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int ACC_COLS = BN;
+    static constexpr int SF_COLS_A = SF_ATOMS * 4;
+    static constexpr int SF_COLS_B = SF_ATOMS * 4 * (BN / 128);
+    static constexpr int SF_COL0 = 2 * ACC_COLS;
+    static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+    static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+    static_assert(!SCALED || BN == 128, "block-scaled tiles use one 128-row scale atom for B");
+};
+
+struct Params {
+    const uint32_t *a_offsets;
+    const uint32_t *a_sf_offsets;
+    const int32_t *expert_ids;
+    int num_groups, num_experts;
+    int64_t total_rows, scale_rows_total;
+    int N, K;
+    const float *a_scales, *b_scales;
+    const uint8_t *a_sf, *b_sf;
+    const float *expert_scales;
+    const float *out_tensor_scale;
+    uint16_t *c;
+    uint8_t *c_packed, *c_sf;
+    uint32_t *err;
+};
+
+struct Tile {
+    int g, mb, nb;
+};
+
+__device__ __forceinline__ Tile decode_tile(const uint32_t *prefix, int G, uint32_t t, int NB) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    uint32_t local = t - prefix[lo];
+    Tile r;
+    r.g = lo;
+    r.mb = (int)(local / (uint32_t)NB);
+    r.nb = (int)(local % (uint32_t)NB);
+    return r;
+}
+
+// Tiles of group g (0 when the group is empty or its offsets / expert id /
+// scale rows are unusable; those errors are reported by CTA 0 only).
+template <class C, int EPI>
+__device__ __forceinline__ uint32_t group_tiles(const Params &p, int g, int NB, bool report) {
+    uint32_t r0 = __ldg(p.a_offsets + g), r1 = __ldg(p.a_offsets + g + 1);
+    int e = __ldg(p.expert_ids + g);
+    if (r1 < r0 || (int64_t)r1 > p.total_rows) {
+        if (report) set_error(p.err, MOEQ_DEVERR_BAD_OFFSETS);
+        return 0;
+    }
+    if (e < 0 || e >= p.num_experts) {
+        if (report) set_error(p.err, MOEQ_DEVERR_BAD_EXPERT);
+        return 0;
+    }
+    uint32_t rows = r1 - r0;
+    if (C::SCALED || EPI == kSwiglu) {
+        uint32_t s0 = __ldg(p.a_sf_offsets + g), s1 = __ldg(p.a_sf_offsets + g + 1);
+        uint32_t need = (rows + 127u) & ~127u;
+        if ((s0 & 127u) || s1 < s0 || s1 - s0 < need || (int64_t)s1 > p.scale_rows_total) {
+            if (report) set_error(p.err, MOEQ_DEVERR_SCALE_ROWS);
+            return 0;
+        }
+    }
+    return (rows + C::BM - 1) / C::BM * (uint32_t)NB;
+}
+
+// Waits for a phase with a bound but without consulting the abort flag;
+// used only to drain in-flight asynchronous work before the CTA exits.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    uint32_t a = smem_u32(bar);
+    long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) break;
+    }
+}
+
+template <class C, int KIND, int EPI>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[C::STAGES];
+    __shared__ uint64_t empty_bar[C::STAGES];
+    __shared__ uint64_t tfull_bar[2];
+    __shared__ uint64_t tempty_bar[2];
+    __shared__ uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ uint32_t prefix[kMaxGroups + 1];
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.num_groups;
+    const int NB = (p.N + C::BN - 1) / C::BN;
+    volatile int *abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], C::EPI_WARPS);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        prefix[0] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+        prefix[g + 1] = group_tiles<C, EPI>(p, g, NB, blockIdx.x == 0);
+    __syncthreads();
+    if (warp == 0) {  // inclusive prefix over prefix[1..G]
+        uint32_t carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            int g = base + lane;
+            uint32_t v = g < G ? prefix[g + 1] : 0u;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (g < G) prefix[g + 1] = carry + v;
+            carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t total = prefix[G];
+    const uint32_t tmem = tmem_slot;
+    const int KT = p.K / C::BK;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_a = policy_evict_last();
+            const uint64_t pol_b = policy_evict_last();
+            const int64_t kv_atoms = C::SCALED ? (int64_t)p.K / C::SF_VEC / 4 : 0;
+            const int nrb = (p.N + 127) / 128;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;       // stages with a load issued
+            uint32_t issued_par = 0;   // phase parity of that load
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const Tile tl = decode_tile(prefix, G, t, NB);
+                const int e = __ldg(p.expert_ids + tl.g);
+                const int row0 = (int)__ldg(p.a_offsets + tl.g) + tl.mb * C::BM;
+                const int n0 = tl.nb * C::BN;
+                int64_t sfa0 = 0, sfb0 = 0;
+                if (C::SCALED) {
+                    sfa0 = ((int64_t)(__ldg(p.a_sf_offsets + tl.g) >> 7) + tl.mb) * kv_atoms;
+                    sfb0 = ((int64_t)e * nrb + n0 / 128) * kv_atoms;
+                }
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_v, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * C::STAGE_BYTES;
+                    uint8_t *sb = sa + C::A_BYTES;
+                    mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+                    tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
+                    tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
+                    if (C::SCALED) {
+                        uint8_t *ssfa = sb + C::B_BYTES;
+                        uint8_t *ssfb = ssfa + C::SFA_BYTES;
+                        bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
+                                  C::SFA_BYTES, &full_bar[stage]);
+                        bulk_load(ssfb, p.b_sf + (sfb0 + (int64_t)kt * C::SF_ATOMS) * 512,
+                                  C::SFB_BYTES, &full_bar[stage]);
+                    }
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // let every issued copy land before the CTA can exit
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued & (1u << s)) mbar_drain(&full_bar[s], (issued_par >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+                const uint32_t buf = it & 1u;
+                const uint32_t aph = (it >> 1) & 1u;
+                if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_v, p.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + buf * C::ACC_COLS;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&full_bar[stage], phase, abort_v, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + C::A_BYTES;
+                    const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
+                    const uint32_t tsfb = tsfa + C::SF_COLS_A;
+                    if (C::SCALED) {
+                        const uint32_t ssfa = sb + C::B_BYTES;
+                        const uint32_t ssfb = ssfa + C::SFA_BYTES;
+#pragma unroll
+                        for (int i = 0; i < C::SF_ATOMS; ++i) {
+                            tmem_cp_sf_atom(tsfa + 4 * i, sdesc_sf_atom(ssfa + 512 * i));
+                            tmem_cp_sf_atom(tsfb + 4 * i, sdesc_sf_atom(ssfb + 512 * i));
+                        }
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                        const uint64_t ad = sdesc_sw128(sa + ks * 32);
+                        const uint64_t bd = sdesc_sw128(sb + ks * 32);
+                        const uint32_t acc = (kt | ks) ? 1u : 0u;
+                        if (KIND == kFp8Rowwise) {
+                            mma_f8f6f4(d, ad, bd, idesc_f8_e4m3(C::BM, C::BN), acc);
+                        } else if (KIND == kNvfp4) {
+                            mma_nvf4(d, ad, bd, idesc_nvf4(C::BM, C::BN), tsfa + 4 * ks,
+                                     tsfb + 4 * ks, acc);
+                        } else {
+                            mma_mxf8(d, ad, bd, idesc_mxf8_e4m3(C::BM, C::BN, ks), tsfa, tsfb,
+                                     acc);
+                        }
+                    }
+                    tc_commit(&empty_bar[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit(&tfull_bar[buf]);
+            }
+            // every tcgen05 operation issued here completes before TMEM is freed
+            tc_commit(&drain_bar);
+            mbar_drain(&drain_bar, 0);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        uint32_t it = 0;
+        float inv_out = 0.0f;
+        for (uint32_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const uint32_t buf = it & 1u;
+            const uint32_t aph = (it >> 1) & 1u;
+            const Tile tl = decode_tile(prefix, G, t, NB);
+            const int e = __ldg(p.expert_ids + tl.g);
+            const uint32_t r0 = __ldg(p.a_offsets + tl.g);
+            const uint32_t rg = __ldg(p.a_offsets + tl.g + 1) - r0;
+            const uint32_t lrow = (uint32_t)(tl.mb * C::BM + quad * 32 + lane);
+            const bool valid = lrow < rg;
+            const int64_t row = (int64_t)r0 + lrow;
+            const int n0 = tl.nb * C::BN;
+            float rs = 1.0f;
+            if (KIND == kFp8Rowwise) {
+                rs = valid ? __ldg(p.a_scales + row) : 0.0f;
+            } else if (p.expert_scales) {
+                rs = __ldg(p.expert_scales + e);
+            }
+            if (EPI == kSwiglu) inv_out = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + e));
+            if (!mbar_wait(&tfull_bar[buf], aph, abort_v, p.err)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + lane_off + buf * C::ACC_COLS;
+            uint32_t sfword = 0;
+#pragma unroll 1
+            for (int ch = 0; ch < C::BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ch * 32, r);
+                tmem_ld_wait();
+                if (ch == C::BN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                }
+                const int nc = n0 + ch * 32;
+                if (EPI == kBf16) {
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int n = nc + j * 8;
+                            if (n >= p.N) break;
+                            float bs[8];
+                            if (KIND == kFp8Rowwise) {
+                                const float4 *bp =
+                                    reinterpret_cast<const float4 *>(p.b_scales + (int64_t)e * p.N + n);
+                                float4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
+                                bs[0] = b0.x; bs[1] = b0.y; bs[2] = b0.z; bs[3] = b0.w;
+                                bs[4] = b1.x; bs[5] = b1.y; bs[6] = b1.z; bs[7] = b1.w;
+                            }
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float v0 = __uint_as_float(r[j * 8 + 2 * i]);
+                                float v1 = __uint_as_float(r[j * 8 + 2 * i + 1]);
+                                if (KIND == kFp8Rowwise) {
+                                    v0 = __fmul_rn(__fmul_rn(v0, rs), bs[2 * i]);
+                                    v1 = __fmul_rn(__fmul_rn(v1, rs), bs[2 * i + 1]);
+                                } else {
+                                    v0 = __fmul_rn(v0, rs);
+                                    v1 = __fmul_rn(v1, rs);
+                                }
+                                w[i] = f32_to_bf16_bits(v0) | (f32_to_bf16_bits(v1) << 16);
+                            }
+                            st_global_v4(p.c + row * p.N + n, w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                } else {
+                    // SwiGLU on (gate, up) column pairs, then one NVFP4 block
+                    float h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float gt = bf16_bits_to_f32(
+                            f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i]), rs)));
+                        float up = bf16_bits_to_f32(
+                            f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i + 1]), rs)));
+                        h[i] = __fmul_rn(silu_spec(gt), up);
+                    }
+                    float m = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(h[i]));
+                    const Nvfp4Scale s = nvfp4_block_scale(m, inv_out);
+                    float lo8[8], hi8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        lo8[i] = h[i];
+                        hi8[i] = h[8 + i];
+                    }
+                    const uint32_t c0 = nvfp4_codes8(lo8, s.r);
+                    const uint32_t c1 = nvfp4_codes8(hi8, s.r);
+                    if (valid)
+                        *reinterpret_cast<uint2 *>(p.c_packed + row * (p.N / 4) + nc / 4) =
+                            make_uint2(c0, c1);
+                    sfword |= s.code << (8 * (ch & 3));
+                    if ((ch & 3) == 3) {
+                        const int64_t prow = (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow;
+                        const int64_t kv_atoms = p.N / 128;
+                        *reinterpret_cast<uint32_t *>(
+                            p.c_sf + sf_word_offset(prow, (nc - 96) / 128, kv_atoms)) =
+                            valid ? sfword : 0u;
+                        sfword = 0;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// uint8 tensor map with 128-byte swizzled boxes of box_rows x 128 bytes.
+bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides, cuuint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint32_t box[3] = {128, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base),
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+template <int KIND, int EPI, int BN, int STAGES>
+cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
+    using C = Cfg<KIND, EPI, BN, STAGES>;
+    const int64_t kbytes = KIND == kNvfp4 ? a.K / 2 : a.K;
+    const int64_t T = a.groups.total_rows;
+    const int64_t E = a.groups.num_experts;
+    CUtensorMap tA, tB;
+    cuuint64_t da[2] = {(cuuint64_t)kbytes, (cuuint64_t)T};
+    cuuint64_t sa[1] = {(cuuint64_t)kbytes};
+    cuuint64_t db[3] = {(cuuint64_t)kbytes, (cuuint64_t)a.N, (cuuint64_t)E};
+    cuuint64_t sb[2] = {(cuuint64_t)kbytes, (cuuint64_t)(kbytes * a.N)};
+    if (!make_map(&tA, a.a, 2, da, sa, C::BM)) return cudaErrorInvalidValue;
+    if (!make_map(&tB, a.b, 3, db, sb, C::BN)) return cudaErrorInvalidValue;
+    Params p;
+    p.a_offsets = a.groups.row_offsets;
+    p.a_sf_offsets = a.groups.scales_offsets;
+    p.expert_ids = a.groups.expert_ids;
+    p.num_groups = a.groups.num_groups;
+    p.num_experts = a.groups.num_experts;
+    p.total_rows = T;
+    p.scale_rows_total = a.groups.scale_rows_total;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.a_scales = a.a_scales;
+    p.b_scales = a.b_scales;
+    p.a_sf = a.a_sf;
+    p.b_sf = a.b_sf;
+    p.expert_scales = a.expert_scales;
+    p.out_tensor_scale = a.out_tensor_scale;
+    p.c = reinterpret_cast<uint16_t *>(a.c);
+    p.c_packed = a.c_packed;
+    p.c_sf = a.c_sf;
+    p.err = a.err;
+    const int64_t nb = (a.N + BN - 1) / BN;
+    const int64_t tiles_ub = (T / C::BM + a.groups.num_groups) * nb;
+    const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
+    auto kern = grouped_gemm_kernel<C, KIND, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
+    if (a.kind == kFp8Rowwise && a.epi == kBf16) {
+        if (a.N >= 256) return run_gemm<kFp8Rowwise, kBf16, 256, 4>(a, s);
+        return run_gemm<kFp8Rowwise, kBf16, 64, 8>(a, s);
+    }
+    if (a.kind == kNvfp4 && a.epi == kBf16) return run_gemm<kNvfp4, kBf16, 128, 5>(a, s);
+    if (a.kind == kNvfp4 && a.epi == kSwiglu) return run_gemm<kNvfp4, kSwiglu, 128, 5>(a, s);
+    if (a.kind == kMxfp8 && a.epi == kBf16) return run_gemm<kMxfp8, kBf16, 128, 6>(a, s);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace moeq

@@ -1,0 +1,59 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel
+// translation units.  Host-only declarations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moeq {
+
+struct GroupArgs {
+    const uint32_t *row_offsets;     // [G+1]
+    const uint32_t *scales_offsets;  // [G+1] or null
+    const int32_t *expert_ids;       // [G]
+    int32_t num_groups;
+    int32_t num_experts;
+    int64_t total_rows;
+    int64_t scale_rows_total;
+};
+
+cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const GroupArgs &g,
+                              float *tensor_scale_out, uint32_t *err, cudaStream_t s);
+
+cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,
+                            uint8_t *scales, const float *tensor_scale, const GroupArgs &g,
+                            uint32_t *err, cudaStream_t s);
+
+cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_offsets,
+                                  int32_t num_groups, cudaStream_t s);
+
+cudaError_t launch_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf, const void *y, int64_t I,
+                                   const float *out_tensor_scale, const GroupArgs &g,
+                                   uint32_t *err, cudaStream_t s);
+
+// Grouped GEMMs.  kind: 0 = FP8 rowwise, 1 = NVFP4 block-scaled,
+// 2 = MXFP8 block-scaled.  epi: 0 = bf16 out, 1 = fused SwiGLU + NVFP4.
+struct GemmArgs {
+    int kind;
+    int epi;
+    GroupArgs groups;
+    int64_t N, K;
+    const uint8_t *a, *b;
+    const float *a_scales, *b_scales;      // FP8 rowwise
+    const uint8_t *a_sf, *b_sf;            // block-scaled
+    const float *expert_scales;            // block-scaled (null = 1)
+    const float *out_tensor_scale;         // fused SwiGLU
+    void *c;                               // bf16 out
+    uint8_t *c_packed, *c_sf;              // fused SwiGLU out
+    int32_t max_tokens_per_expert;
+    uint32_t *err;
+};
+
+// Returns cudaErrorNotSupported for shapes without a built kernel.
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
+
+// Maximum number of groups the GEMM scheduler accepts.
+constexpr int kMaxGroups = 1024;
+
+}  // namespace moeq

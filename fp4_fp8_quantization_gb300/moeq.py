@@ -1,0 +1,188 @@
+"""Python binding of the moeq C ABI (``include/moeq.h``).
+
+Argument marshalling only: each function checks that the tensors it is given
+are CUDA tensors of the documented dtype and layout, passes their device
+pointers and sizes to the function of the same name in ``libmoeq.so`` on the
+current CUDA stream (or ``stream``), and raises ``MoeqError`` on a non-OK
+status.  Every step of the computation runs in the library's CUDA kernels;
+there is no other implementation, and importing a function whose library is
+missing raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoeq.so")
+_lib = None
+
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
+STATUS = {0: "MOEQ_OK", 1: "MOEQ_ERR_INVALID_ARG", 2: "MOEQ_ERR_UNSUPPORTED",
+          3: "MOEQ_ERR_CUDA", 4: "MOEQ_ERR_DEVICE"}
+DEVERR_BAD_OFFSETS, DEVERR_BAD_EXPERT, DEVERR_SCALE_ROWS, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_P, _I64, _I32, _U32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)
+_SIGNATURES = {
+    "moeq_grouped_amax_scale": [_P, _I64, _I64, _I64, _P, _P, _P, _I32, _I32, _P],
+    "moeq_grouped_quantize": [_I32, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P,
+                              _I32, _I32, _I32, _P],
+    "moeq_padded_scale_offsets": [_P, _P, _I32, _P],
+    "moeq_grouped_matmul_rowwise_fp8": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                        _I32, _I32, _I32, _P],
+    "moeq_grouped_matmul_blockscaled": [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                        _I64, _I64, _I32, _I32, _I32, _P],
+    "moeq_swiglu_quantize": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P],
+    "moeq_grouped_matmul_swiglu": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                   _I64, _I32, _I32, _I32, _P],
+    "moeq_get_device_error": [_P, _U32P],
+    "moeq_clear_device_error": [_P],
+    "moeq_last_cuda_error": [],
+    "moeq_status_string": [ctypes.c_int],
+}
+EXPORTS = tuple(_SIGNATURES)
+
+
+class MoeqError(RuntimeError):
+    def __init__(self, fn, status):
+        code = lib().moeq_last_cuda_error() if status == 3 else 0
+        super().__init__(f"{fn}: {STATUS.get(status, status)}" + (f" (cuda error {code})" if code else ""))
+        self.status = status
+
+
+def lib():
+    """The loaded libmoeq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "python -m fp4_fp8_quantization_gb300.build")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, args in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.moeq_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _call(fn, *args):
+    st = getattr(lib(), fn)(*args)
+    if st != 0:
+        raise MoeqError(fn, st)
+
+
+def _fmt(fmt):
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+_U8 = (torch.uint8, torch.float8_e4m3fn)
+_U32 = (torch.uint32, torch.int32)
+
+
+def grouped_amax_scale(inp, row_offsets, expert_ids, tensor_scale_out, num_experts,
+                       num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_amax_scale", _ptr(inp, torch.bfloat16, "inp"), inp.stride(0),
+          inp.shape[0], inp.shape[1], _ptr(row_offsets, _U32), _ptr(expert_ids, torch.int32),
+          _ptr(tensor_scale_out, torch.float32), num_experts, G, _stream(stream))
+
+
+def grouped_quantize(fmt, inp, out, scales, row_offsets, scales_offsets, expert_ids,
+                     tensor_scale, num_experts, scale_rows_total, max_tokens_per_expert=0,
+                     num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_quantize", _fmt(fmt), _ptr(inp, torch.bfloat16, "inp"), inp.stride(0),
+          inp.shape[0], inp.shape[1], _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"),
+          scale_rows_total, _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32),
+          _ptr(expert_ids, torch.int32), _ptr(tensor_scale, torch.float32), num_experts,
+          max_tokens_per_expert, G, _stream(stream))
+
+
+def padded_scale_offsets(row_offsets, scales_offsets, num_active_experts=None, stream=None):
+    G = row_offsets.numel() - 1 if num_active_experts is None else num_active_experts
+    _call("moeq_padded_scale_offsets", _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32), G,
+          _stream(stream))
+
+
+def grouped_matmul_rowwise_fp8(c, a, b, a_scales, b_scales, a_offsets, expert_ids,
+                               max_tokens_per_expert=0, num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    E, N, K = b.shape
+    _call("moeq_grouped_matmul_rowwise_fp8", _ptr(c, torch.bfloat16, "c"), _ptr(a, _U8, "a"),
+          _ptr(b, _U8, "b"), _ptr(a_scales, torch.float32), _ptr(b_scales, torch.float32),
+          _ptr(a_offsets, _U32), _ptr(expert_ids, torch.int32), a.shape[0], N, K, E,
+          max_tokens_per_expert, G, _stream(stream))
+
+
+def grouped_matmul_blockscaled(fmt, c, a, a_sf, b, b_sf, expert_scales, a_offsets,
+                               a_scales_offsets, expert_ids, N, K, scale_rows_total,
+                               max_tokens_per_expert=0, num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_matmul_blockscaled", _fmt(fmt), _ptr(c, torch.bfloat16, "c"),
+          _ptr(a, _U8, "a"), _ptr(a_sf, _U8, "a_sf"), _ptr(b, _U8, "b"), _ptr(b_sf, _U8, "b_sf"),
+          _ptr(expert_scales, torch.float32), _ptr(a_offsets, _U32), _ptr(a_scales_offsets, _U32),
+          _ptr(expert_ids, torch.int32), a.shape[0], scale_rows_total, N, K, b.shape[0],
+          max_tokens_per_expert, G, _stream(stream))
+
+
+def swiglu_quantize(c_packed, c_sf, y, out_tensor_scale, a_offsets, a_scales_offsets,
+                    expert_ids, num_experts, scale_rows_total, max_tokens_per_expert=0,
+                    num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_swiglu_quantize", _ptr(c_packed, _U8), _ptr(c_sf, _U8),
+          _ptr(y, torch.bfloat16, "y"), _ptr(out_tensor_scale, torch.float32),
+          _ptr(a_offsets, _U32), _ptr(a_scales_offsets, _U32), _ptr(expert_ids, torch.int32),
+          y.shape[0], scale_rows_total, y.shape[1] // 2, num_experts, max_tokens_per_expert, G,
+          _stream(stream))
+
+
+def grouped_matmul_swiglu(c_packed, c_sf, a, a_sf, b, b_sf, expert_scales, out_tensor_scale,
+                          a_offsets, a_scales_offsets, expert_ids, I, K, scale_rows_total,
+                          max_tokens_per_expert=0, num_active_experts=None, stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_matmul_swiglu", _ptr(c_packed, _U8), _ptr(c_sf, _U8), _ptr(a, _U8),
+          _ptr(a_sf, _U8), _ptr(b, _U8), _ptr(b_sf, _U8), _ptr(expert_scales, torch.float32),
+          _ptr(out_tensor_scale, torch.float32), _ptr(a_offsets, _U32),
+          _ptr(a_scales_offsets, _U32), _ptr(expert_ids, torch.int32), a.shape[0],
+          scale_rows_total, I, K, b.shape[0], max_tokens_per_expert, G, _stream(stream))
+
+
+def get_device_error(stream=None):
+    """Sticky device error bits (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    st = lib().moeq_get_device_error(_stream(stream), ctypes.byref(v))
+    if st not in (0, 4):
+        raise MoeqError("moeq_get_device_error", st)
+    return v.value
+
+
+def clear_device_error(stream=None):
+    _call("moeq_clear_device_error", _stream(stream))
+
+
+def sf_bytes(rows, kv):
+    """Bytes of a tiled block-scale buffer for [rows, kv] logical scales."""
+    return (rows + 127) // 128 * ((kv + 3) // 4) * 512

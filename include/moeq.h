@@ -1,0 +1,242 @@
+/*
+ * moeq: grouped mixture-of-experts low-precision kernels for one GB300 GPU
+ * (sm_103a).  C ABI.
+ *
+ * Conventions shared by every call below
+ * --------------------------------------
+ * - Every pointer is a DEVICE pointer the caller owns (allocated with
+ *   cudaMalloc, PyTorch, ...).  The library never allocates, frees or
+ *   synchronises inside a compute call; each call only enqueues kernels on
+ *   `stream` (a cudaStream_t; NULL = the legacy default stream) and returns.
+ *   Pointers must be 16-byte aligned unless stated otherwise.
+ * - Ragged expert groups ("grouped_matmul_rowwise_dynamic_scaled_fp8", Args
+ *   a_offsets / expert_ids): group g = 0..num_active_experts-1 owns rows
+ *   [offsets[g], offsets[g+1]) and uses expert expert_ids[g] (any order,
+ *   need not be sorted or unique).  offsets are uint32 [G+1], expert_ids are
+ *   int32 [G].  Empty groups write nothing.  Rows outside every group are
+ *   never written.
+ * - Padded scale rows ("max.nn.moe.NvMxf4f8Strategy", grouped_quantize:
+ *   "padded scale alignment"; "grouped_quantize_dynamic_scaled_fp4_async_kernel",
+ *   scales_offsets): the block scales of group g live in logical scale rows
+ *   [scales_offsets[g], scales_offsets[g+1]); scales_offsets[g] must be a
+ *   multiple of 128 and leave room for ceil(r_g / 128) * 128 rows.
+ *   moeq_padded_scale_offsets() builds the tightest such offsets.
+ * - Block-scale layout (the tensor core's tiled layout; the pages leave it
+ *   open): logical scales [rows, Kv] (Kv = K / block) are stored as 512-byte
+ *   atoms of 128 rows x 4 columns; byte (r, c) of an atom is at
+ *   (r % 32) * 16 + (r / 32) * 4 + c; atom (rb, kb) starts at
+ *   (rb * ceil(Kv / 4) + kb) * 512.  Weight scales are one such buffer per
+ *   expert, each ceil(N / 128) * ceil(Kv / 4) * 512 bytes.
+ * - FP4 elements are packed two per byte, the lower-k element in the low
+ *   nibble.
+ * - num_active_experts == 0 (or zero total rows) is MOEQ_OK and launches
+ *   nothing.  max_tokens_per_expert is a sizing hint ("Max tokens routed to
+ *   any active expert"): it picks launch shapes only, and groups larger than
+ *   it are still computed in full.
+ * - Errors.  Bad host arguments return MOEQ_ERR_INVALID_ARG before anything
+ *   is launched (this includes a missing NVFP4 scale tensor, the pages'
+ *   ValueError of prepare_swiglu_operands).  A shape or format that is not
+ *   built returns MOEQ_ERR_UNSUPPORTED.  A launch failure returns
+ *   MOEQ_ERR_CUDA (see moeq_last_cuda_error()).  Bad device-side data
+ *   (non-monotone offsets, an expert id outside [0, num_experts), offsets
+ *   past the buffers, a wait that timed out) never faults the GPU: the
+ *   affected group is skipped and a sticky bit is set in the device error
+ *   word, read with moeq_get_device_error().
+ */
+#ifndef MOEQ_H
+#define MOEQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moeq_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    MOEQ_OK = 0,
+    MOEQ_ERR_INVALID_ARG = 1,
+    MOEQ_ERR_UNSUPPORTED = 2,
+    MOEQ_ERR_CUDA = 3,
+    MOEQ_ERR_DEVICE = 4
+} moeq_status;
+
+/* Quantized formats ("max.nn.moe.NvMxf4f8Strategy", is_nvfp4; the kernel of
+ * "grouped_quantize_dynamic_scaled_fp4_async_kernel" quantizes to
+ * NVFP4 / MXFP4 / MXFP8).
+ *   NVFP4: E2M1 elements, 16-element blocks, E4M3 block scale, fp32
+ *          per-expert tensor scale.
+ *   MXFP4: E2M1 elements, 32-element blocks, E8M0 block scale.
+ *   MXFP8: E4M3 elements, 32-element blocks, E8M0 block scale. */
+typedef enum { MOEQ_NVFP4 = 0, MOEQ_MXFP4 = 1, MOEQ_MXFP8 = 2 } moeq_format;
+
+/* Device error word bits (sticky until moeq_clear_device_error). */
+#define MOEQ_DEVERR_BAD_OFFSETS 0x1u /* non-monotone or out-of-range offsets */
+#define MOEQ_DEVERR_BAD_EXPERT 0x2u  /* expert id outside [0, num_experts)   */
+#define MOEQ_DEVERR_SCALE_ROWS 0x4u  /* scale offsets unaligned / too small  */
+#define MOEQ_DEVERR_TIMEOUT 0x8u     /* a pipeline wait gave up (~1 s)       */
+
+/* Per-expert NVFP4 tensor scale of the activations
+ * ("grouped_quantize_dynamic_scaled_fp4_async_kernel": sf_tensor, the
+ * per-expert tensor-wise scale factor, is a read-only input; this call
+ * produces it).  tensor_scale_out[e] = fp32(amax_e / 2688), 2688 = 6 * 448,
+ * amax_e = max |in| over all rows of all groups routed to expert e; experts
+ * with no rows or an all-zero input get 1.0.
+ *   in            bf16 [total_rows, K], row stride in_row_stride elements.
+ *   row_offsets   uint32 [G+1]; expert_ids int32 [G].
+ *   tensor_scale_out  fp32 [num_experts], fully overwritten.
+ * K must be a multiple of 8; in_row_stride a multiple of 8, >= K. */
+moeq_status moeq_grouped_amax_scale(const void *in, int64_t in_row_stride,
+                                    int64_t total_rows, int64_t K,
+                                    const uint32_t *row_offsets,
+                                    const int32_t *expert_ids,
+                                    float *tensor_scale_out,
+                                    int32_t num_experts,
+                                    int32_t num_active_experts,
+                                    moeq_stream_t stream);
+
+/* Grouped activation quantizer ("grouped_quantize_dynamic_scaled_fp4_async_kernel":
+ * each block of work finds its expert by binary search on row_offsets /
+ * scales_offsets and quantizes that expert's BF16 rows; "max.nn.moe.NvMxf4f8Strategy",
+ * grouped_quantize).
+ *   in            bf16 [total_rows, K], row stride in_row_stride elements.
+ *   out           NVFP4 / MXFP4: [total_rows, K/2] packed; MXFP8: [total_rows, K].
+ *   scales        tiled block-scale buffer of scale_rows_total logical rows
+ *                 x K/16 (NVFP4) or K/32 (MX) columns.  For group g the rows
+ *                 [scales_offsets[g], scales_offsets[g] + r_g) get the scales of
+ *                 its rows and the rows up to scales_offsets[g] + ceil(r_g/128)*128
+ *                 are zeroed; any further rows and rows >= scales_offsets[G]
+ *                 are untouched.
+ *   tensor_scale  fp32 [num_experts] raw (dequantization-direction) scale s_e
+ *                 (NVFP4 only, required; ignored for MX).
+ * Per block (NVFP4): inv = 1/s_e; sb = E4M3((amax * inv) / 6);
+ * q = E2M1(x * (inv / sb)), all zero when sb == 0.  MX: scale code
+ * c = clamp(floor(log2 amax) - emax + 127, 0, 254) (emax 8 for E4M3, 2 for
+ * E2M1); q = elem(x * 2^(127-c)); an all-zero block is all +0 with c = 0.
+ * All rounding is to nearest even, saturating.  K must be a multiple of 128;
+ * scale_rows_total a multiple of 128. */
+moeq_status moeq_grouped_quantize(moeq_format fmt, const void *in,
+                                  int64_t in_row_stride, int64_t total_rows,
+                                  int64_t K, uint8_t *out, uint8_t *scales,
+                                  int64_t scale_rows_total,
+                                  const uint32_t *row_offsets,
+                                  const uint32_t *scales_offsets,
+                                  const int32_t *expert_ids,
+                                  const float *tensor_scale,
+                                  int32_t num_experts,
+                                  int32_t max_tokens_per_expert,
+                                  int32_t num_active_experts,
+                                  moeq_stream_t stream);
+
+/* scales_offsets[g] = sum_{h<g} ceil((row_offsets[h+1]-row_offsets[h]) / 128) * 128,
+ * g = 0..G (uint32 [G+1], device).  The tightest padding accepted by the
+ * calls above. */
+moeq_status moeq_padded_scale_offsets(const uint32_t *row_offsets,
+                                      uint32_t *scales_offsets,
+                                      int32_t num_active_experts,
+                                      moeq_stream_t stream);
+
+/* Grouped rowwise-scaled FP8 matmul ("grouped_matmul_rowwise_dynamic_scaled_fp8",
+ * description and Args):
+ *   c[t, n] = bf16( (sum_k a[t,k] * b[expert_ids[g], n, k]) * a_scales[t]
+ *                   * b_scales[expert_ids[g], n] )
+ * accumulated in fp32 by the tensor cores, the two scales applied once after
+ * the reduction (acc * a_scale first, then * b_scale), round to nearest even.
+ *   c         bf16 [total_tokens, N]
+ *   a         E4M3 [total_tokens, K]
+ *   b         E4M3 [num_experts, N, K] (K innermost; "transpose_b must be True")
+ *   a_scales  fp32 [total_tokens];  b_scales fp32 [num_experts, N]
+ * K % 128 == 0, N % 16 == 0. */
+moeq_status moeq_grouped_matmul_rowwise_fp8(
+    void *c, const uint8_t *a, const uint8_t *b, const float *a_scales,
+    const float *b_scales, const uint32_t *a_offsets,
+    const int32_t *expert_ids, int64_t total_tokens, int64_t N, int64_t K,
+    int32_t num_experts, int32_t max_tokens_per_expert,
+    int32_t num_active_experts, moeq_stream_t stream);
+
+/* Grouped block-scaled matmul with per-expert epilogue scales
+ * ("max.nn.moe.NvMxf4f8Strategy", grouped_matmul: "grouped NVIDIA
+ * block-scaled matmul with per-expert scales"; expert_scales are the
+ * "per-expert matmul-epilogue scaling factors"):
+ *   c[t, n] = bf16( expert_scales[e] * sum_k (qa[t,k] * sa[t,k/v]) * (qb[e,n,k] * sb[e,n,k/v]) )
+ * with e = expert_ids[g], v = 16 (NVFP4) or 32 (MXFP8).
+ *   a      NVFP4: packed [total_tokens, K/2]; MXFP8: [total_tokens, K]
+ *   a_sf   tiled scales, scale_rows_total rows; row t of group g uses
+ *          scale row a_scales_offsets[g] + (t - a_offsets[g])
+ *   b      NVFP4: packed [num_experts, N, K/2]; MXFP8: [num_experts, N, K]
+ *   b_sf   per-expert tiled scales (see the layout above)
+ *   expert_scales  fp32 [num_experts]; required for NVFP4, NULL means 1 for MX.
+ * NVFP4: K % 256 == 0; MXFP8: K % 128 == 0; N % 128 == 0.  MXFP4 returns
+ * MOEQ_ERR_UNSUPPORTED. */
+moeq_status moeq_grouped_matmul_blockscaled(
+    moeq_format fmt, void *c, const uint8_t *a, const uint8_t *a_sf,
+    const uint8_t *b, const uint8_t *b_sf, const float *expert_scales,
+    const uint32_t *a_offsets, const uint32_t *a_scales_offsets,
+    const int32_t *expert_ids, int64_t total_tokens, int64_t scale_rows_total,
+    int64_t N, int64_t K, int32_t num_experts, int32_t max_tokens_per_expert,
+    int32_t num_active_experts, moeq_stream_t stream);
+
+/* Chained SwiGLU + NVFP4 requantization ("max.nn.moe.NvMxf4f8Strategy",
+ * fused_silu_quantize: applies the gated activation then quantizes; the
+ * SiLU-output scale is passed raw and inverted inside, as
+ * prepare_swiglu_operands requires).
+ *   y      bf16 [total_tokens, 2I]: column 2j = gate_j, 2j+1 = up_j
+ *   h_j    = silu(gate_j) * up_j in fp32, silu(g) = g / (1 + exp(-g)) with the
+ *            library's own deterministic fp32 exp (Cody-Waite reduction,
+ *            degree-7 Taylor polynomial, no fused multiply-add)
+ *   c_packed  NVFP4 [total_tokens, I/2];  c_sf tiled scales [scale_rows_total
+ *            rows x I/16], padded per expert exactly like moeq_grouped_quantize
+ *   out_tensor_scale  fp32 [num_experts] raw s_e (required).
+ * I % 64 == 0. */
+moeq_status moeq_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf,
+                                 const void *y, const float *out_tensor_scale,
+                                 const uint32_t *a_offsets,
+                                 const uint32_t *a_scales_offsets,
+                                 const int32_t *expert_ids,
+                                 int64_t total_tokens,
+                                 int64_t scale_rows_total, int64_t I,
+                                 int32_t num_experts,
+                                 int32_t max_tokens_per_expert,
+                                 int32_t num_active_experts,
+                                 moeq_stream_t stream);
+
+/* Fused grouped NVFP4 matmul + SwiGLU + NVFP4 requantization in one kernel
+ * ("max.nn.moe.NvMxf4f8Strategy", grouped_matmul_swiglu: equivalent to
+ * grouped_matmul followed by fused_silu_quantize; its (c_packed,
+ * c_swiglu_scales) match the chained path byte for byte with a bf16
+ * rounding where the chained path has a bf16 tensor).
+ * Computes, with no bf16 tensor in memory, exactly
+ *   moeq_grouped_matmul_blockscaled(NVFP4, y, ...) ; moeq_swiglu_quantize(..., y, ...)
+ * and writes the same bytes.  b is [num_experts, 2I, K/2] with gate/up rows
+ * interleaved (row 2j = gate_j, row 2j+1 = up_j); b_sf its per-expert tiled
+ * scales.  expert_scales and out_tensor_scale are required.
+ * K % 256 == 0, I % 64 == 0. */
+moeq_status moeq_grouped_matmul_swiglu(
+    uint8_t *c_packed, uint8_t *c_sf, const uint8_t *a, const uint8_t *a_sf,
+    const uint8_t *b, const uint8_t *b_sf, const float *expert_scales,
+    const float *out_tensor_scale, const uint32_t *a_offsets,
+    const uint32_t *a_scales_offsets, const int32_t *expert_ids,
+    int64_t total_tokens, int64_t scale_rows_total, int64_t I, int64_t K,
+    int32_t num_experts, int32_t max_tokens_per_expert,
+    int32_t num_active_experts, moeq_stream_t stream);
+
+/* Reads the sticky device error word of the current device (MOEQ_DEVERR_*
+ * bits) after synchronising `stream`.  Returns MOEQ_ERR_DEVICE when any bit
+ * is set, MOEQ_OK otherwise. */
+moeq_status moeq_get_device_error(moeq_stream_t stream, uint32_t *bits);
+
+/* Clears the device error word of the current device (enqueued on stream). */
+moeq_status moeq_clear_device_error(moeq_stream_t stream);
+
+/* The cudaError_t of the last MOEQ_ERR_CUDA on this thread (0 if none). */
+int moeq_last_cuda_error(void);
+
+/* Static string naming a status. */
+const char *moeq_status_string(moeq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ_H */

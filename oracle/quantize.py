@@ -19,8 +19,9 @@ Sources.
     floor rule (``mx_quantize_blocks``).
   - Padded scale rows: expert group g owns logical scale rows
     [scales_offsets[g], scales_offsets[g+1]); its r_g data rows come first,
-    the remaining rows of that range are written as zero bytes.  Rows at or
-    beyond scales_offsets[G] are not touched.
+    then the rows up to the next multiple of 128 (ceil(r_g / 128) * 128 rows
+    in all) are written as zero bytes.  Any further rows of the range, and
+    rows at or beyond scales_offsets[G], are not touched.
 
 All float32 steps are numpy float32 operations: one IEEE binary32 operation
 each, round-to-nearest-even, no fused multiply-add.
@@ -169,7 +170,8 @@ def grouped_quantize(fmt, x, row_offsets, scales_offsets, expert_ids,
         p0, p1 = int(scales_offsets[g]), int(scales_offsets[g + 1])
         rg = r1 - r0
         assert rg >= 0 and p1 - p0 >= rg and p0 % 128 == 0
-        logical = np.zeros((p1 - p0, kv), np.uint8)
+        padded = (rg + 127) // 128 * 128
+        logical = np.zeros((padded, kv), np.uint8)
         if rg > 0:
             s = None
             if fmt == "nvfp4":
@@ -177,7 +179,7 @@ def grouped_quantize(fmt, x, row_offsets, scales_offsets, expert_ids,
             q, sc = quantize_rows(fmt, x[r0:r1], s)
             out[r0:r1] = q
             logical[:rg] = sc
-        rr, cc = np.meshgrid(np.arange(p0, p1), np.arange(kv), indexing="ij")
+        rr, cc = np.meshgrid(np.arange(p0, p0 + padded), np.arange(kv), indexing="ij")
         scales[L.sf_offset(rr, cc, kv)] = logical
     return out, scales
 

@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/moeq.h declares, and rejects bad host arguments before launching
+anything (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp4_fp8_quantization_gb300 import moeq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moeq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moeq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moeq._LIB_PATH):
+        from fp4_fp8_quantization_gb300 import build
+        build.build()
+    return moeq.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moeq.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code, name in moeq.STATUS.items():
+        assert lib.moeq_status_string(code).decode() == name
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)          # 16-byte aligned, never dereferenced
+ODD = P(0x10004)
+
+
+def test_quantize_rejects_bad_host_arguments(lib):
+    f = lib.moeq_grouped_quantize
+    ok = dict(fmt=0, inp=FAKE, stride=256, rows=10, K=256, out=FAKE, sf=FAKE, srows=128,
+              ro=FAKE, so=FAKE, ids=FAKE, ts=FAKE, E=4, mt=10, G=2, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["fmt"], a["inp"], a["stride"], a["rows"], a["K"], a["out"], a["sf"],
+                 a["srows"], a["ro"], a["so"], a["ids"], a["ts"], a["E"], a["mt"], a["G"], a["s"])
+
+    assert call(K=100) == 1                # K % 128
+    assert call(stride=200) == 1           # stride < K
+    assert call(srows=100) == 1            # scale rows % 128
+    assert call(ts=None) == 1              # NVFP4 without tensor scale (ValueError analogue)
+    assert call(fmt=7) == 1
+    assert call(ro=None) == 1
+    assert call(E=0) == 1
+    assert call(G=-1) == 1
+    assert call(inp=ODD) == 1              # misaligned
+    assert call(G=0) == 0                  # no groups: OK, nothing launched
+    assert call(fmt=2, ts=None, G=0) == 0  # MX needs no tensor scale
+
+
+def test_gemms_reject_bad_host_arguments(lib):
+    r = lib.moeq_grouped_matmul_rowwise_fp8
+    #        c     a     b     sa    sb    ao    ids   T   N    K    E  mt  G  stream
+    assert r(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 100, 2, 8, 2, None) == 1  # K
+    assert r(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 72, 128, 2, 8, 2, None) == 1  # N % 16
+    assert r(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 64, 64, 128, 2, 8, 2, None) == 1  # b
+    assert r(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 128, 2, 8, 2000, None) == 2
+    assert r(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 128, 2, 8, 0, None) == 0
+    bs = lib.moeq_grouped_matmul_blockscaled
+    args = [0] + [FAKE] * 9 + [64, 128, 128, 512, 2, 8, 2, None]
+    a = list(args); a[0] = 1                                 # MXFP4 GEMM: not built
+    assert bs(*a) == 2
+    a = list(args); a[0] = 0; a[6] = None                    # NVFP4 without expert scales
+    assert bs(*a) == 1
+    a = list(args); a[0] = 0; a[13] = 384                    # NVFP4 needs K % 256
+    assert bs(*a) == 1
+    a = list(args); a[0] = 2; a[6] = None; a[12] = 192       # N % 128
+    assert bs(*a) == 1
+    sw = lib.moeq_grouped_matmul_swiglu
+    sargs = [FAKE] * 11 + [64, 128, 64, 512, 2, 8, 2, None]
+    a = list(sargs); a[7] = None                             # missing SiLU-output scale
+    assert sw(*a) == 1
+    a = list(sargs); a[13] = 96                              # I % 64
+    assert sw(*a) == 1
+    q = lib.moeq_swiglu_quantize
+    assert q(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 64, 128, 64, 2, 8, 2, None) == 1
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 2, 8, 2, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moeq, "_lib", None)
+    monkeypatch.setattr(moeq, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        moeq.lib()

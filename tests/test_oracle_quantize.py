@@ -140,7 +140,24 @@ def test_grouped_quantize_semantics(fmt):
         q, sc = Q.quantize_rows(fmt, x[r0:r1], ts[e] if fmt == "nvfp4" else None)
         assert np.array_equal(out[r0:r1], q)
         assert np.array_equal(logical[p0:p0 + (r1 - r0)], sc)
-        assert not logical[p0 + (r1 - r0):p1].any()          # padding rows zero
+        padded = (r1 - r0 + 127) // 128 * 128
+        assert not logical[p0 + (r1 - r0):p0 + padded].any()  # padding rows zero
+        assert np.all(logical[p0 + padded:p1] == 0x5A)       # slack rows untouched
+
+
+def test_grouped_quantize_slack_scale_rows_untouched():
+    """Offsets with more than the tight padding: only ceil128(r_g) rows of a
+    group's scale range are written."""
+    rng = np.random.default_rng(14)
+    x = F.round_bf16(rng.normal(0, 1, (10, 128))).astype(np.float32)
+    ro = np.array([0, 3, 10], np.uint32)
+    so = np.array([0, 256, 512], np.uint32)
+    sf0 = np.full(L.physical_bytes(512, 8), 0x5A, np.uint8)
+    _, sf = Q.grouped_quantize("nvfp4", x, ro, so, np.array([0, 1], np.int32),
+                               np.ones(2, np.float32), scales=sf0, scale_rows_total=512)
+    lg = L.unswizzle(sf, 512, 8)
+    assert not lg[3:128].any() and np.all(lg[128:256] == 0x5A)
+    assert not lg[263:384].any() and np.all(lg[384:512] == 0x5A)
 
 
 def test_grouped_quantize_group_permutation():
