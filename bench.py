@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     p.add_argument("--no-parts", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained"],
+                   help="run only --warmup + --steps launches of one kernel on a small case "
+                        "(inputs larger than L2, under 1 GB) for a profiler; no JSON line")
     return p.parse_args()
 
 
@@ -508,8 +511,74 @@ def run_moeq(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """Small cases for profiler captures: same kernels and launch shapes as
+    the bench, fewer experts / rows (inputs still larger than L2)."""
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    dev = "cuda"
+    u32 = lambda a: torch.from_numpy(np.asarray(a, np.uint32).view(np.int32)).to(dev)
+    if args.profile in ("fused", "chained", "quantize"):
+        # 32 experts, 4096 tokens top-8 -> 32768 rows, K 4096, I 1536
+        counts = synth.routing_counts(4096, 8, 32, seed=0)
+        ro, ids = synth.ragged_groups(counts)
+        T, N, rows = int(ro[-1]), 2 * I4, int(sum((int(c) + 127) // 128 * 128 for c in counts))
+        ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+        so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
+        moeq.padded_scale_offsets(ro_d, so_d)
+        if args.profile == "quantize":
+            x = synth.bf16_normal((T, K4), 1.0, seed=1, device=dev)
+            ts = synth.uniform((32,), 0.001, 0.002, seed=2, device=dev)
+            q = torch.empty((T, K4 // 2), dtype=torch.uint8, device=dev)
+            sf = torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8, device=dev)
+            fn = lambda: moeq.grouped_quantize("nvfp4", x, q, sf, ro_d, so_d, ids_d, ts, 32, rows)
+        else:
+            a = synth.random_fp4_packed((T, K4 // 2), seed=1, device=dev)
+            asf = synth.random_bytes(moeq.sf_bytes(rows, K4 // 16), 0x20, 0x30, seed=2, device=dev)
+            b = synth.random_fp4_packed((32, N, K4 // 2), seed=3, device=dev)
+            bsf = synth.random_bytes(32 * moeq.sf_bytes(N, K4 // 16), 0x18, 0x28, seed=4,
+                                     device=dev)
+            es = synth.uniform((32,), 0.5, 2.0, seed=5, device=dev)
+            ots = synth.uniform((32,), 1.0, 4.0, seed=6, device=dev)
+            c = torch.empty((T, I4 // 2), dtype=torch.uint8, device=dev)
+            csf = torch.empty(moeq.sf_bytes(rows, I4 // 16), dtype=torch.uint8, device=dev)
+            if args.profile == "fused":
+                fn = lambda: moeq.grouped_matmul_swiglu(c, csf, a, asf, b, bsf, es, ots, ro_d,
+                                                        so_d, ids_d, I4, K4, rows)
+            else:
+                y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+                fn = lambda: moeq.grouped_matmul_blockscaled("nvfp4", y, a, asf, b, bsf, es, ro_d,
+                                                             so_d, ids_d, N, K4, rows)
+    else:
+        # FP8 rowwise: 16 experts, 2048 tokens top-8 Zipf -> 16384 rows (fp8) or
+        # decode-shaped 64 experts, 16 tokens top-8 -> 128 rows; K 7168, N 4096
+        if args.profile == "fp8":
+            counts = synth.routing_counts(2048, 8, 16, seed=0, zipf_s=1.1)
+            E = 16
+        else:
+            counts = synth.routing_counts(16, 8, 64, seed=0)
+            E = 64
+        ro, ids = synth.ragged_groups(counts)
+        T, N, K = int(ro[-1]), 4096, 7168
+        a, sa = synth.fp8_rowwise((T, K), 1.0, seed=1, device=dev)
+        b, sb = synth.fp8_rowwise((E, N, K), 0.02, seed=2, device=dev)
+        c = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+        fn = lambda: moeq.grouped_matmul_rowwise_fp8(c, a, b, sa, sb.reshape(E, N), ro_d, ids_d,
+                                                     int(counts.max()))
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    assert moeq.get_device_error() == 0
+    print(f"profile case {args.profile}: {args.warmup} + {args.steps} launches ok")
+
+
 def main():
     args = parse_args()
+    if args.profile:
+        torch.cuda.set_device(0)
+        run_profile_case(args)
+        return
     rank, world = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -110,10 +110,10 @@ __device__ __forceinline__ float exp_spec(float x) {
     const float c5 = 0.008333333767950534820556640625f;  // fp32(1/5!)
     const float c6 = 0.001388888922519981861114501953125f;    // fp32(1/6!)
     const float c7 = 0.0001984127011382952332496643066406f;   // fp32(1/7!)
-    if (x >= 89.0f) return __int_as_float(0x7f800000);
-    if (x <= -104.0f) return 0.0f;
-    float n = rintf(__fmul_rn(x, kLog2e));
-    float f = __fsub_rn(x, __fmul_rn(n, kLn2Hi));
+    // Branch-free: evaluate on the clamped argument, select the limits after.
+    const float xc = fminf(fmaxf(x, -104.0f), 89.0f);
+    float n = rintf(__fmul_rn(xc, kLog2e));
+    float f = __fsub_rn(xc, __fmul_rn(n, kLn2Hi));
     f = __fsub_rn(f, __fmul_rn(n, kLn2Lo));
     float p = c7;
     p = __fadd_rn(__fmul_rn(p, f), c6);
@@ -128,7 +128,9 @@ __device__ __forceinline__ float exp_spec(float x) {
     int n2 = ni - n1;
     float s1 = __int_as_float((n1 + 127) << 23);
     float s2 = __int_as_float((n2 + 127) << 23);
-    return __fmul_rn(__fmul_rn(p, s1), s2);
+    float r = __fmul_rn(__fmul_rn(p, s1), s2);
+    r = (x >= 89.0f) ? __int_as_float(0x7f800000) : r;
+    return (x <= -104.0f) ? 0.0f : r;
 }
 
 __device__ __forceinline__ float silu_spec(float g) {
@@ -395,6 +397,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Streaming 16-byte load of read-once data (not kept in L1).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 // --------------------------------------------------------- global stores

@@ -38,38 +38,45 @@ namespace {
 enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2 };
 enum Epi { kBf16 = 0, kSwiglu = 1 };
 
-template <int KIND, int EPI, int BN_, int STAGES_>
+template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_>
 struct Cfg {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
+    static constexpr int ACC_BUFS = ACC_BUFS_;                  // TMEM accumulators
     static constexpr int BK_BYTES = 128;                        // one 128B swizzle row
     static constexpr int ELEMS_PER_BYTE = KIND == kNvfp4 ? 2 : 1;
     static constexpr int BK = BK_BYTES * ELEMS_PER_BYTE;        // K elements per stage
     static constexpr int KSTEPS = 4;                            // 32 bytes of K per MMA
     static constexpr bool SCALED = KIND != kFp8Rowwise;
     static constexpr int SF_VEC = KIND == kNvfp4 ? 16 : 32;
+    static constexpr int RB = BN >= 128 ? BN / 128 : 1;         // 128-row scale blocks of B
     static constexpr int SF_ATOMS = SCALED ? BK / SF_VEC / 4 : 0;   // atoms per 128 rows per stage
     static constexpr int SF_ATOM_BYTES = 512;
     static constexpr int A_BYTES = BM * BK_BYTES;
     static constexpr int B_BYTES = BN * BK_BYTES;
     static constexpr int SFA_BYTES = SF_ATOMS * SF_ATOM_BYTES;
-    static constexpr int SFB_BYTES = SF_ATOMS * SF_ATOM_BYTES * (BN / 128);
+    static constexpr int SFB_BYTES = SF_ATOMS * SF_ATOM_BYTES * RB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int TX_BYTES = STAGE_BYTES;
-    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int EPI_GROUPS = EPI_WARPS / 4;            // epilogue warps per TMEM quarter
+    static constexpr int COLS_W = BN / EPI_GROUPS;              // accumulator columns per warp
+    static constexpr int CHUNKS_W = COLS_W / 32;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int ACC_COLS = BN;
     static constexpr int SF_COLS_A = SF_ATOMS * 4;
-    static constexpr int SF_COLS_B = SF_ATOMS * 4 * (BN / 128);
-    static constexpr int SF_COL0 = 2 * ACC_COLS;
+    static constexpr int SF_COLS_B = SF_ATOMS * 4 * RB;
+    static constexpr int SF_COL0 = ACC_BUFS * ACC_COLS;
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
     static constexpr int TMEM_COLS = 512;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
-    static_assert(!SCALED || BN == 128, "block-scaled tiles use one 128-row scale atom for B");
+    static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale atoms");
+    static_assert(EPI_WARPS % 4 == 0 && COLS_W % 32 == 0 && COLS_W >= 32, "epilogue split");
+    static_assert(ACC_BUFS == 2 || CHUNKS_W <= 4, "single accumulator drains TMEM to registers");
+    static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
 };
 
 struct Params {
@@ -142,6 +149,89 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Epilogue of one 32-column accumulator chunk of this thread's row.
+//   bf16 out: c[row, n] = bf16(acc * scale(s)); FP8 rowwise applies
+//             a_scale (rs) then b_scale[e, n]; block-scaled the expert scale.
+//   SwiGLU:   16 (gate, up) pairs -> 16 h -> one NVFP4 block; returns the
+//             E4M3 scale code, writes the 8 packed bytes.
+template <class C, int KIND, int EPI>
+__device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32_t (&r)[32],
+                                                   int nc, int e, int64_t row, bool valid,
+                                                   float rs, float inv_out) {
+    if (EPI == kBf16) {
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = nc + j * 8;
+                if (n >= p.N) break;
+                float bs[8];
+                if (KIND == kFp8Rowwise) {
+                    const float4 *bp =
+                        reinterpret_cast<const float4 *>(p.b_scales + (int64_t)e * p.N + n);
+                    float4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
+                    bs[0] = b0.x; bs[1] = b0.y; bs[2] = b0.z; bs[3] = b0.w;
+                    bs[4] = b1.x; bs[5] = b1.y; bs[6] = b1.z; bs[7] = b1.w;
+                }
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v0 = __uint_as_float(r[j * 8 + 2 * i]);
+                    float v1 = __uint_as_float(r[j * 8 + 2 * i + 1]);
+                    if (KIND == kFp8Rowwise) {
+                        v0 = __fmul_rn(__fmul_rn(v0, rs), bs[2 * i]);
+                        v1 = __fmul_rn(__fmul_rn(v1, rs), bs[2 * i + 1]);
+                    } else {
+                        v0 = __fmul_rn(v0, rs);
+                        v1 = __fmul_rn(v1, rs);
+                    }
+                    w[i] = f32_to_bf16_bits(v0) | (f32_to_bf16_bits(v1) << 16);
+                }
+                st_global_v4(p.c + row * p.N + n, w[0], w[1], w[2], w[3]);
+            }
+        }
+        return 0u;
+    } else {
+        float h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float gt = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i]), rs)));
+            float up =
+                bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i + 1]), rs)));
+            h[i] = __fmul_rn(silu_spec(gt), up);
+        }
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(h[i]));
+        const Nvfp4Scale s = nvfp4_block_scale(m, inv_out);
+        float lo8[8], hi8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo8[i] = h[i];
+            hi8[i] = h[8 + i];
+        }
+        const uint32_t c0 = nvfp4_codes8(lo8, s.r);
+        const uint32_t c1 = nvfp4_codes8(hi8, s.r);
+        if (valid)
+            *reinterpret_cast<uint2 *>(p.c_packed + row * (p.N / 4) + nc / 4) = make_uint2(c0, c1);
+        return s.code;
+    }
+}
+
+// Stores the NVFP4 scale bytes of `nblk` consecutive blocks (nblk = 1, 2 or
+// 4 chunks of 32 accumulator columns) starting at accumulator column nc0.
+__device__ __forceinline__ void store_sf_bytes(const Params &p, int64_t prow, int nc0,
+                                               uint32_t bytes, int nblk) {
+    const int64_t kv_atoms = p.N / 128;
+    const int blk = nc0 / 32;  // first NVFP4 block of the output row
+    uint8_t *w = p.c_sf + sf_word_offset(prow, blk / 4, kv_atoms) + (blk & 3);
+    if (nblk == 4)
+        *reinterpret_cast<uint32_t *>(w) = bytes;
+    else if (nblk == 2)
+        *reinterpret_cast<uint16_t *>(w) = (uint16_t)bytes;
+    else
+        *w = (uint8_t)bytes;
+}
+
 template <class C, int KIND, int EPI>
 __global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -149,8 +239,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ uint64_t empty_bar[C::STAGES];
-    __shared__ uint64_t tfull_bar[2];
-    __shared__ uint64_t tempty_bar[2];
+    __shared__ uint64_t tfull_bar[C::ACC_BUFS];
+    __shared__ uint64_t tempty_bar[C::ACC_BUFS];
     __shared__ uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -171,7 +261,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&empty_bar[s], 1);
         }
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::ACC_BUFS; ++b) {
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], C::EPI_WARPS);
         }
@@ -230,10 +320,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int row0 = (int)__ldg(p.a_offsets + tl.g) + tl.mb * C::BM;
                 const int n0 = tl.nb * C::BN;
                 int64_t sfa0 = 0, sfb0 = 0;
+                int rbs = 1;  // scale row-blocks of B present in this tile
                 if (C::SCALED) {
                     sfa0 = ((int64_t)(__ldg(p.a_sf_offsets + tl.g) >> 7) + tl.mb) * kv_atoms;
                     sfb0 = ((int64_t)e * nrb + n0 / 128) * kv_atoms;
+                    rbs = min(C::RB, nrb - n0 / 128);
                 }
+                const uint32_t tx = C::A_BYTES + C::B_BYTES + C::SFA_BYTES +
+                                    (uint32_t)rbs * C::SF_ATOMS * C::SF_ATOM_BYTES;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_v, p.err)) {
                         ok = false;
@@ -241,7 +335,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     uint8_t *sa = smem + stage * C::STAGE_BYTES;
                     uint8_t *sb = sa + C::A_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+                    mbar_arrive_expect_tx(&full_bar[stage], C::SCALED ? tx : (uint32_t)(C::A_BYTES + C::B_BYTES));
                     tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
                     tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
                     if (C::SCALED) {
@@ -249,8 +343,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         uint8_t *ssfb = ssfa + C::SFA_BYTES;
                         bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
                                   C::SFA_BYTES, &full_bar[stage]);
-                        bulk_load(ssfb, p.b_sf + (sfb0 + (int64_t)kt * C::SF_ATOMS) * 512,
-                                  C::SFB_BYTES, &full_bar[stage]);
+                        for (int rb = 0; rb < rbs; ++rb)
+                            bulk_load(ssfb + rb * C::SF_ATOMS * 512,
+                                      p.b_sf + (sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
+                                      C::SF_ATOMS * 512, &full_bar[stage]);
                     }
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -273,8 +369,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (uint32_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
-                const uint32_t buf = it & 1u;
-                const uint32_t aph = (it >> 1) & 1u;
+                const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
+                const uint32_t aph = C::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
                 if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_v, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * C::ACC_COLS;
@@ -289,12 +385,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
                     const uint32_t tsfb = tsfa + C::SF_COLS_A;
                     if (C::SCALED) {
+                        // A atom ks -> columns 4 ks; B atom (rb, ks) -> columns
+                        // 4 (ks RB + rb), so each MMA step reads 4 RB
+                        // consecutive columns covering its N rows.
                         const uint32_t ssfa = sb + C::B_BYTES;
                         const uint32_t ssfb = ssfa + C::SFA_BYTES;
 #pragma unroll
                         for (int i = 0; i < C::SF_ATOMS; ++i) {
                             tmem_cp_sf_atom(tsfa + 4 * i, sdesc_sf_atom(ssfa + 512 * i));
-                            tmem_cp_sf_atom(tsfb + 4 * i, sdesc_sf_atom(ssfb + 512 * i));
+#pragma unroll
+                            for (int rb = 0; rb < C::RB; ++rb)
+                                tmem_cp_sf_atom(tsfb + 4 * (i * C::RB + rb),
+                                                sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
                         }
                     }
 #pragma unroll
@@ -306,7 +408,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             mma_f8f6f4(d, ad, bd, idesc_f8_e4m3(C::BM, C::BN), acc);
                         } else if (KIND == kNvfp4) {
                             mma_nvf4(d, ad, bd, idesc_nvf4(C::BM, C::BN), tsfa + 4 * ks,
-                                     tsfb + 4 * ks, acc);
+                                     tsfb + 4 * C::RB * ks, acc);
                         } else {
                             mma_mxf8(d, ad, bd, idesc_mxf8_e4m3(C::BM, C::BN, ks), tsfa, tsfb,
                                      acc);
@@ -327,12 +429,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else {
         // ------------------------------------------------ epilogue
         const int quad = warp & 3;
+        const int cgrp = (warp - 2) >> 2;            // column group of this warp
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t it = 0;
-        float inv_out = 0.0f;
         for (uint32_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const uint32_t buf = it & 1u;
-            const uint32_t aph = (it >> 1) & 1u;
+            const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
+            const uint32_t aph = C::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
             const Tile tl = decode_tile(prefix, G, t, NB);
             const int e = __ldg(p.expert_ids + tl.g);
             const uint32_t r0 = __ldg(p.a_offsets + tl.g);
@@ -340,8 +442,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t lrow = (uint32_t)(tl.mb * C::BM + quad * 32 + lane);
             const bool valid = lrow < rg;
             const int64_t row = (int64_t)r0 + lrow;
-            const int n0 = tl.nb * C::BN;
-            float rs = 1.0f;
+            const int ncol0 = tl.nb * C::BN + cgrp * C::COLS_W;
+            float rs = 1.0f, inv_out = 0.0f;
             if (KIND == kFp8Rowwise) {
                 rs = valid ? __ldg(p.a_scales + row) : 0.0f;
             } else if (p.expert_scales) {
@@ -350,86 +452,58 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (EPI == kSwiglu) inv_out = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + e));
             if (!mbar_wait(&tfull_bar[buf], aph, abort_v, p.err)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem + lane_off + buf * C::ACC_COLS;
-            uint32_t sfword = 0;
-#pragma unroll 1
-            for (int ch = 0; ch < C::BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tbase + ch * 32, r);
+            const uint32_t tbase = tmem + lane_off + buf * C::ACC_COLS + cgrp * C::COLS_W;
+            uint32_t sfbytes = 0;
+            if (ncol0 >= p.N) {
+                // this warp's columns lie past N (last n-block of an N that is
+                // not a multiple of BN): nothing to read or write
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                continue;
+            }
+            if (C::ACC_BUFS == 1) {
+                // drain this warp's columns to registers, free TMEM, then compute
+                uint32_t r[C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W][32];
+#pragma unroll
+                for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
+                    tmem_ld32(tbase + ch * 32, r[ch]);
                 tmem_ld_wait();
-                if (ch == C::BN / 32 - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-                }
-                const int nc = n0 + ch * 32;
-                if (EPI == kBf16) {
-                    if (valid) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int n = nc + j * 8;
-                            if (n >= p.N) break;
-                            float bs[8];
-                            if (KIND == kFp8Rowwise) {
-                                const float4 *bp =
-                                    reinterpret_cast<const float4 *>(p.b_scales + (int64_t)e * p.N + n);
-                                float4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
-                                bs[0] = b0.x; bs[1] = b0.y; bs[2] = b0.z; bs[3] = b0.w;
-                                bs[4] = b1.x; bs[5] = b1.y; bs[6] = b1.z; bs[7] = b1.w;
-                            }
-                            uint32_t w[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                float v0 = __uint_as_float(r[j * 8 + 2 * i]);
-                                float v1 = __uint_as_float(r[j * 8 + 2 * i + 1]);
-                                if (KIND == kFp8Rowwise) {
-                                    v0 = __fmul_rn(__fmul_rn(v0, rs), bs[2 * i]);
-                                    v1 = __fmul_rn(__fmul_rn(v1, rs), bs[2 * i + 1]);
-                                } else {
-                                    v0 = __fmul_rn(v0, rs);
-                                    v1 = __fmul_rn(v1, rs);
-                                }
-                                w[i] = f32_to_bf16_bits(v0) | (f32_to_bf16_bits(v1) << 16);
-                            }
-                            st_global_v4(p.c + row * p.N + n, w[0], w[1], w[2], w[3]);
+                for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
+                    sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
+                                                            valid, rs, inv_out)
+                               << (8 * ch);
+            } else {
+#pragma unroll 1
+                for (int ch = 0; ch < C::CHUNKS_W; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + ch * 32, r);
+                    tmem_ld_wait();
+                    if (ch == C::CHUNKS_W - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                    }
+                    const uint32_t code = epilogue_chunk<C, KIND, EPI>(
+                        p, r, ncol0 + ch * 32, e, row, valid, rs, inv_out);
+                    if (EPI == kSwiglu) {
+                        sfbytes |= code << (8 * (ch & 3));
+                        if ((ch & 3) == 3) {
+                            store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow,
+                                           ncol0 + (ch - 3) * 32, valid ? sfbytes : 0u, 4);
+                            sfbytes = 0;
                         }
                     }
-                } else {
-                    // SwiGLU on (gate, up) column pairs, then one NVFP4 block
-                    float h[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float gt = bf16_bits_to_f32(
-                            f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i]), rs)));
-                        float up = bf16_bits_to_f32(
-                            f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i + 1]), rs)));
-                        h[i] = __fmul_rn(silu_spec(gt), up);
-                    }
-                    float m = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(h[i]));
-                    const Nvfp4Scale s = nvfp4_block_scale(m, inv_out);
-                    float lo8[8], hi8[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        lo8[i] = h[i];
-                        hi8[i] = h[8 + i];
-                    }
-                    const uint32_t c0 = nvfp4_codes8(lo8, s.r);
-                    const uint32_t c1 = nvfp4_codes8(hi8, s.r);
-                    if (valid)
-                        *reinterpret_cast<uint2 *>(p.c_packed + row * (p.N / 4) + nc / 4) =
-                            make_uint2(c0, c1);
-                    sfword |= s.code << (8 * (ch & 3));
-                    if ((ch & 3) == 3) {
-                        const int64_t prow = (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow;
-                        const int64_t kv_atoms = p.N / 128;
-                        *reinterpret_cast<uint32_t *>(
-                            p.c_sf + sf_word_offset(prow, (nc - 96) / 128, kv_atoms)) =
-                            valid ? sfword : 0u;
-                        sfword = 0;
-                    }
                 }
+            }
+            if (EPI == kSwiglu && (C::ACC_BUFS == 1 || C::CHUNKS_W < 4)) {
+                const int nblk = C::CHUNKS_W < 4 ? C::CHUNKS_W : 4;
+                store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow, ncol0,
+                               valid ? sfbytes : 0u, nblk);
             }
         }
     }
@@ -490,9 +564,9 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int KIND, int EPI, int BN, int STAGES>
+template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS>;
     const int64_t kbytes = KIND == kNvfp4 ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
@@ -536,14 +610,53 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 
 }  // namespace
 
+// Tile configurations (compile-time).  NVFP4: 128x256 tiles with one TMEM
+// accumulator (256 columns) plus per-stage scale slots; the epilogue drains
+// its columns to registers and frees TMEM before computing, so the next
+// tile's MMAs start at once.  FP8: 128x256 tiles, two accumulators.
+#ifndef MOEQ_FP8_BN
+#define MOEQ_FP8_BN 256
+#endif
+#ifndef MOEQ_FP8_STAGES
+#define MOEQ_FP8_STAGES 4
+#endif
+#ifndef MOEQ_FP8_EPI_WARPS
+#define MOEQ_FP8_EPI_WARPS 4
+#endif
+#ifndef MOEQ_FP4_BN
+#define MOEQ_FP4_BN 256
+#endif
+#ifndef MOEQ_FP4_STAGES
+#define MOEQ_FP4_STAGES 4
+#endif
+#ifndef MOEQ_FP4_ACC_BUFS
+#define MOEQ_FP4_ACC_BUFS 1
+#endif
+#ifndef MOEQ_FP4_EPI_WARPS
+#define MOEQ_FP4_EPI_WARPS 8
+#endif
+#ifndef MOEQ_SWIGLU_EPI_WARPS
+#define MOEQ_SWIGLU_EPI_WARPS 16
+#endif
+#ifndef MOEQ_MX8_STAGES
+#define MOEQ_MX8_STAGES 6
+#endif
+
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.kind == kFp8Rowwise && a.epi == kBf16) {
-        if (a.N >= 256) return run_gemm<kFp8Rowwise, kBf16, 256, 4>(a, s);
-        return run_gemm<kFp8Rowwise, kBf16, 64, 8>(a, s);
+        if (a.N >= 256)
+            return run_gemm<kFp8Rowwise, kBf16, MOEQ_FP8_BN, MOEQ_FP8_STAGES, 2,
+                            MOEQ_FP8_EPI_WARPS>(a, s);
+        return run_gemm<kFp8Rowwise, kBf16, 64, 8, 2, 4>(a, s);
     }
-    if (a.kind == kNvfp4 && a.epi == kBf16) return run_gemm<kNvfp4, kBf16, 128, 5>(a, s);
-    if (a.kind == kNvfp4 && a.epi == kSwiglu) return run_gemm<kNvfp4, kSwiglu, 128, 5>(a, s);
-    if (a.kind == kMxfp8 && a.epi == kBf16) return run_gemm<kMxfp8, kBf16, 128, 6>(a, s);
+    if (a.kind == kNvfp4 && a.epi == kBf16)
+        return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
+                        MOEQ_FP4_EPI_WARPS>(a, s);
+    if (a.kind == kNvfp4 && a.epi == kSwiglu)
+        return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
+                        MOEQ_SWIGLU_EPI_WARPS>(a, s);
+    if (a.kind == kMxfp8 && a.epi == kBf16)
+        return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;
 }
 

@@ -120,7 +120,16 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ 
         int e = __ldg(g.expert_ids + gi);
         const uint4 *src = reinterpret_cast<const uint4 *>(in + row * stride);
         uint32_t m = 0;
-        for (int64_t c = lane; c < K / 8; c += 32) m = max(m, bf16_abs_max8(__ldg(src + c)));
+        const int64_t n16 = K / 8;
+        int64_t c = lane;
+        for (; c + 7 * 32 < n16; c += 8 * 32) {  // 8 independent loads in flight
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = ld_stream(src + c + u * 32);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m = max(m, bf16_abs_max8(v[u]));
+        }
+        for (; c < n16; c += 32) m = max(m, bf16_abs_max8(ld_stream(src + c)));
         m = __reduce_max_sync(0xFFFFFFFFu, m);
         if (e != cur_e) {
             if (cur_e >= 0 && lane == 0 && cur_m) atomicMax(amax_bits + cur_e, cur_m << 16);
@@ -178,14 +187,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
     // only lanes 0..15 active (they still take part in the shuffles).
     const int nchunks = (int)((p.K + 255) / 256);
     const int lanes_last = (int)((p.K / 8) - (int64_t)(nchunks - 1) * 32);
-    constexpr int U = 4;
+    constexpr int U = 8;  // 8 x 16 bytes in flight per lane
     for (int c0 = 0; c0 < nchunks; c0 += U) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             v[u] = make_uint4(0u, 0u, 0u, 0u);
             if (c0 + u < nchunks && (c0 + u < nchunks - 1 || lane < lanes_last))
-                v[u] = __ldg(src + (int64_t)(c0 + u) * 32 + lane);
+                v[u] = ld_stream(src + (int64_t)(c0 + u) * 32 + lane);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -275,13 +284,27 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
     const float inv = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + __ldg(p.g.expert_ids + gi)));
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;
-    for (int64_t h0 = 0; h0 < nh; h0 += 256) {
+    constexpr int U = 3;  // 256-h steps whose loads are issued together
+    for (int64_t hb = 0; hb < nh; hb += 256 * U) {
+      uint4 v[U][2];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t hl = hb + u * 256 + lane * 8;
+        v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (hl < nh) {
+            v[u][0] = ld_stream(src + hl / 4);
+            v[u][1] = ld_stream(src + hl / 4 + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t h0 = hb + u * 256;
+        if (h0 >= nh) break;
         const int64_t hl = h0 + lane * 8;          // first h of this lane
         const bool active = hl < nh;
         float h[8];
         if (active) {
-            uint4 v0 = __ldg(src + hl / 4);
-            uint4 v1 = __ldg(src + hl / 4 + 1);
+            const uint4 v0 = v[u][0], v1 = v[u][1];
             uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -306,6 +329,7 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
                 *reinterpret_cast<uint32_t *>(
                     p.scales + sf_word_offset(prow, hl / 64, kv_atoms)) = word;
         }
+      }
     }
 }
 
