@@ -38,7 +38,7 @@ namespace {
 enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2 };
 enum Epi { kBf16 = 0, kSwiglu = 1 };
 
-template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_>
+template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_>
 struct Cfg {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -62,7 +62,10 @@ struct Cfg {
     static constexpr int EPI_GROUPS = EPI_WARPS / 4;            // epilogue warps per TMEM quarter
     static constexpr int COLS_W = BN / EPI_GROUPS;              // accumulator columns per warp
     static constexpr int CHUNKS_W = COLS_W / 32;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int SF_WARPS = SCALED ? SF_WARPS_ : 0;      // warps issuing scale copies
+    static constexpr int SF_ITEMS = SF_ATOMS * (1 + RB);         // scale atoms per stage
+    static constexpr int EPI_WARP0 = 2 + SF_WARPS;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr int ACC_COLS = BN;
     static constexpr int SF_COLS_A = SF_ATOMS * 4;
     static constexpr int SF_COLS_B = SF_ATOMS * 4 * RB;
@@ -242,6 +245,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ uint64_t tfull_bar[C::ACC_BUFS];
     __shared__ uint64_t tempty_bar[C::ACC_BUFS];
     __shared__ uint64_t drain_bar;
+    __shared__ uint64_t sf_bar[C::STAGES];     // scale atoms of a stage are in TMEM
+    __shared__ uint64_t sf_drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ uint32_t prefix[kMaxGroups + 1];
@@ -266,6 +271,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&tempty_bar[b], C::EPI_WARPS);
         }
         mbar_init(&drain_bar, 1);
+        mbar_init(&sf_drain_bar, C::SF_WARPS > 0 ? C::SF_WARPS : 1);  // one commit per scale warp
+#pragma unroll
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(&sf_bar[s], C::SF_WARPS > 0 ? C::SF_WARPS : 1);
         abort_flag = 0;
         prefix[0] = 0;
         fence_barrier_init();
@@ -375,7 +383,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + buf * C::ACC_COLS;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&full_bar[stage], phase, abort_v, p.err)) {
+                    // block-scaled: the scale warp signals once the stage's
+                    // operands have landed and its scales are in TMEM
+                    if (!mbar_wait(C::SCALED ? &sf_bar[stage] : &full_bar[stage], phase, abort_v,
+                                   p.err)) {
                         ok = false;
                         break;
                     }
@@ -384,21 +395,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const uint32_t sb = sa + C::A_BYTES;
                     const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
                     const uint32_t tsfb = tsfa + C::SF_COLS_A;
-                    if (C::SCALED) {
-                        // A atom ks -> columns 4 ks; B atom (rb, ks) -> columns
-                        // 4 (ks RB + rb), so each MMA step reads 4 RB
-                        // consecutive columns covering its N rows.
-                        const uint32_t ssfa = sb + C::B_BYTES;
-                        const uint32_t ssfb = ssfa + C::SFA_BYTES;
-#pragma unroll
-                        for (int i = 0; i < C::SF_ATOMS; ++i) {
-                            tmem_cp_sf_atom(tsfa + 4 * i, sdesc_sf_atom(ssfa + 512 * i));
-#pragma unroll
-                            for (int rb = 0; rb < C::RB; ++rb)
-                                tmem_cp_sf_atom(tsfb + 4 * (i * C::RB + rb),
-                                                sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
-                        }
-                    }
 #pragma unroll
                     for (int ks = 0; ks < C::KSTEPS; ++ks) {
                         const uint64_t ad = sdesc_sw128(sa + ks * 32);
@@ -426,10 +422,60 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tc_commit(&drain_bar);
             mbar_drain(&drain_bar, 0);
         }
+    } else if (C::SF_WARPS && warp >= 2 && warp < C::EPI_WARP0) {
+        // ------------------------------------------------ scale copies
+        // Copies each stage's scale atoms shared -> TMEM (tcgen05.cp) ahead of
+        // the MMA thread and publishes them with tcgen05.commit on sf_bar.
+        // A stage's TMEM scale slot is rewritten only after full_bar of its
+        // next use, which the producer can only reach after the MMAs that
+        // read the slot have completed (empty_bar), so the slot is free.
+        const int sfw = warp - 2;
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&full_bar[stage], phase, abort_v, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ssfa =
+                        smem_u32(smem + stage * C::STAGE_BYTES) + C::A_BYTES + C::B_BYTES;
+                    const uint32_t ssfb = ssfa + C::SFA_BYTES;
+                    const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
+                    const uint32_t tsfb = tsfa + C::SF_COLS_A;
+                    // A atom ks -> columns 4 ks; B atom (rb, ks) -> columns
+                    // 4 (ks RB + rb), so each MMA step reads 4 RB
+                    // consecutive columns covering its N rows.  The atoms
+                    // of a stage are dealt round-robin over the scale warps.
+#pragma unroll
+                    for (int j = 0; j < C::SF_ITEMS; ++j) {
+                        if (j % C::SF_WARPS != sfw) continue;
+                        if (j < C::SF_ATOMS) {
+                            tmem_cp_sf_atom(tsfa + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
+                        } else {
+                            const int i = (j - C::SF_ATOMS) / C::RB, rb = (j - C::SF_ATOMS) % C::RB;
+                            tmem_cp_sf_atom(tsfb + 4 * (i * C::RB + rb),
+                                            sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
+                        }
+                    }
+                    tc_commit(&sf_bar[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            tc_commit(&sf_drain_bar);
+            mbar_drain(&sf_drain_bar, 0);
+        }
     } else {
         // ------------------------------------------------ epilogue
         const int quad = warp & 3;
-        const int cgrp = (warp - 2) >> 2;            // column group of this warp
+        const int cgrp = (warp - C::EPI_WARP0) >> 2;  // column group of this warp
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t it = 0;
         for (uint32_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -564,9 +610,9 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS>
+template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS>;
     const int64_t kbytes = KIND == kNvfp4 ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
@@ -638,6 +684,9 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 #ifndef MOEQ_SWIGLU_EPI_WARPS
 #define MOEQ_SWIGLU_EPI_WARPS 16
 #endif
+#ifndef MOEQ_SF_WARPS
+#define MOEQ_SF_WARPS 1
+#endif
 #ifndef MOEQ_MX8_STAGES
 #define MOEQ_MX8_STAGES 6
 #endif
@@ -651,10 +700,10 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     }
     if (a.kind == kNvfp4 && a.epi == kBf16)
         return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_FP4_EPI_WARPS>(a, s);
+                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_SWIGLU_EPI_WARPS>(a, s);
+                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
     if (a.kind == kMxfp8 && a.epi == kBf16)
         return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;
