@@ -84,6 +84,15 @@ __device__ __forceinline__ Nvfp4Scale nvfp4_block_scale(float m, float inv) {
     return s;
 }
 
+// The E4M3 scale code of a block only (the element multiplier is then
+// inv / value(code), which callers may tabulate per code).
+__device__ __forceinline__ Nvfp4Scale nvfp4_block_scale_code(float m, float inv) {
+    Nvfp4Scale s;
+    s.code = e4m3(__fdiv_rn(__fmul_rn(m, inv), 6.0f));
+    s.r = 0.0f;
+    return s;
+}
+
 // Eight elements of a block -> 32 bits of packed codes.
 __device__ __forceinline__ uint32_t nvfp4_codes8(const float (&x)[8], float r) {
     if (r == 0.0f) return 0u;
@@ -241,6 +250,40 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Multicast variants: the box lands at the same shared-memory offset in every
+// CTA of the cluster named in cta_mask and completes on the barrier at the
+// same offset in each of them.
+__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                               int x, int y, int z, uint16_t cta_mask,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
+        "cluster.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_mc(void *dst, const void *src, uint32_t bytes,
+                                             uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
@@ -299,6 +342,16 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// As tc_commit, arriving on the barrier at the same offset in every CTA of
+// the cluster named in cta_mask.
+__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 

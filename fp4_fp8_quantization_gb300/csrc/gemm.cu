@@ -38,9 +38,11 @@ namespace {
 enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2 };
 enum Epi { kBf16 = 0, kSwiglu = 1 };
 
-template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_>
+template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
+          int CM_>
 struct Cfg {
     static constexpr int BM = 128;
+    static constexpr int CM = CM_;  // CTAs per cluster sharing (multicasting) each B tile
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;                  // TMEM accumulators
@@ -80,6 +82,8 @@ struct Cfg {
     static_assert(EPI_WARPS % 4 == 0 && COLS_W % 32 == 0 && COLS_W >= 32, "epilogue split");
     static_assert(ACC_BUFS == 2 || CHUNKS_W <= 4, "single accumulator drains TMEM to registers");
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
+    static_assert(CM == 1 || (CM == 2 && BN % 256 == 0), "multicast splits B into 128-row halves");
+    static constexpr int B_ROWS_CTA = BN / CM;                  // rows of B each CTA loads
 };
 
 struct Params {
@@ -139,7 +143,8 @@ __device__ __forceinline__ uint32_t group_tiles(const Params &p, int g, int NB, 
             return 0;
         }
     }
-    return (rows + C::BM - 1) / C::BM * (uint32_t)NB;
+    // a cluster of CM CTAs takes CM consecutive m-blocks of the group
+    return ((rows + C::BM - 1) / C::BM + C::CM - 1) / C::CM * (uint32_t)NB;
 }
 
 // Waits for a phase with a bound but without consulting the abort flag;
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            mbar_init(&empty_bar[s], C::CM);  // one MMA commit per CTA of the cluster
         }
 #pragma unroll
         for (int b = 0; b < C::ACC_BUFS; ++b) {
@@ -306,9 +311,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Multicast clusters: the peer's barriers must be initialised before any
+    // copy or commit targets them.
+    if (C::CM > 1) cluster_sync();
     const uint32_t total = prefix[G];
     const uint32_t tmem = tmem_slot;
     const int KT = p.K / C::BK;
+    const uint32_t rank = C::CM > 1 ? cluster_ctarank() : 0u;   // m-block within the pair
+    const uint32_t cid = blockIdx.x / C::CM, ncl = gridDim.x / C::CM;
+    constexpr uint16_t kAll = (uint16_t)((1u << C::CM) - 1u);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -322,15 +333,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t issued = 0;       // stages with a load issued
             uint32_t issued_par = 0;   // phase parity of that load
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (uint32_t t = cid; ok && t < total; t += ncl) {
                 const Tile tl = decode_tile(prefix, G, t, NB);
+                const int mb = tl.mb * C::CM + (int)rank;
                 const int e = __ldg(p.expert_ids + tl.g);
-                const int row0 = (int)__ldg(p.a_offsets + tl.g) + tl.mb * C::BM;
+                const int row0 = (int)__ldg(p.a_offsets + tl.g) + mb * C::BM;
                 const int n0 = tl.nb * C::BN;
                 int64_t sfa0 = 0, sfb0 = 0;
                 int rbs = 1;  // scale row-blocks of B present in this tile
                 if (C::SCALED) {
-                    sfa0 = ((int64_t)(__ldg(p.a_sf_offsets + tl.g) >> 7) + tl.mb) * kv_atoms;
+                    // an m-block past the group's end (the second CTA of a
+                    // cluster on a group with an odd m-block count) computes
+                    // discarded rows: point its A scales at a real m-block so
+                    // the bulk copy stays inside the scale buffer
+                    const uint32_t rgp = __ldg(p.a_offsets + tl.g + 1) - __ldg(p.a_offsets + tl.g);
+                    const int mlast = (int)((rgp + C::BM - 1) / C::BM) - 1;
+                    sfa0 = ((int64_t)(__ldg(p.a_sf_offsets + tl.g) >> 7) + min(mb, mlast)) * kv_atoms;
                     sfb0 = ((int64_t)e * nrb + n0 / 128) * kv_atoms;
                     rbs = min(C::RB, nrb - n0 / 128);
                 }
@@ -345,16 +363,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     uint8_t *sb = sa + C::A_BYTES;
                     mbar_arrive_expect_tx(&full_bar[stage], C::SCALED ? tx : (uint32_t)(C::A_BYTES + C::B_BYTES));
                     tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
-                    tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
+                    if (C::CM == 1) {
+                        tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
+                    } else {  // this CTA's half of B, delivered to both CTAs
+                        tma_load_3d_mc(sb + rank * C::B_ROWS_CTA * C::BK_BYTES, &tmB,
+                                       &full_bar[stage], kt * C::BK_BYTES,
+                                       n0 + (int)rank * C::B_ROWS_CTA, e, kAll, pol_b);
+                    }
                     if (C::SCALED) {
                         uint8_t *ssfa = sb + C::B_BYTES;
                         uint8_t *ssfb = ssfa + C::SFA_BYTES;
                         bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
                                   C::SFA_BYTES, &full_bar[stage]);
-                        for (int rb = 0; rb < rbs; ++rb)
-                            bulk_load(ssfb + rb * C::SF_ATOMS * 512,
-                                      p.b_sf + (sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
-                                      C::SF_ATOMS * 512, &full_bar[stage]);
+                        if (C::CM == 1) {
+                            for (int rb = 0; rb < rbs; ++rb)
+                                bulk_load(ssfb + rb * C::SF_ATOMS * 512,
+                                          p.b_sf + (sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
+                                          C::SF_ATOMS * 512, &full_bar[stage]);
+                        } else if ((int)rank < rbs) {  // scale row-block `rank`, to both CTAs
+                            bulk_load_mc(ssfb + rank * C::SF_ATOMS * 512,
+                                         p.b_sf + (sfb0 + rank * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
+                                         C::SF_ATOMS * 512, &full_bar[stage], kAll);
+                        }
                     }
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -376,7 +406,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t phase = 0;
             uint32_t it = 0;
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+            for (uint32_t t = cid; ok && t < total; t += ncl, ++it) {
                 const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
                 const uint32_t aph = C::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
                 if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_v, p.err)) break;
@@ -410,7 +440,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                      acc);
                         }
                     }
-                    tc_commit(&empty_bar[stage]);
+                    if (C::CM == 1)
+                        tc_commit(&empty_bar[stage]);
+                    else  // the stage is free once every CTA of the cluster consumed it
+                        tc_commit_mc(&empty_bar[stage], kAll);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -433,7 +466,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
+            for (uint32_t t = cid; t < total; t += ncl) {
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(&full_bar[stage], phase, abort_v, p.err)) {
@@ -478,14 +511,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int cgrp = (warp - C::EPI_WARP0) >> 2;  // column group of this warp
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint32_t it = 0;
-        for (uint32_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        for (uint32_t t = cid; t < total; t += ncl, ++it) {
             const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
             const uint32_t aph = C::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
             const Tile tl = decode_tile(prefix, G, t, NB);
             const int e = __ldg(p.expert_ids + tl.g);
             const uint32_t r0 = __ldg(p.a_offsets + tl.g);
             const uint32_t rg = __ldg(p.a_offsets + tl.g + 1) - r0;
-            const uint32_t lrow = (uint32_t)(tl.mb * C::BM + quad * 32 + lane);
+            const int mb = tl.mb * C::CM + (int)rank;
+            // scale rows of this m-block exist only if the group reaches it
+            const bool mb_in_group = (uint32_t)mb * C::BM < rg;
+            const uint32_t lrow = (uint32_t)(mb * C::BM + quad * 32 + lane);
             const bool valid = lrow < rg;
             const int64_t row = (int64_t)r0 + lrow;
             const int ncol0 = tl.nb * C::BN + cgrp * C::COLS_W;
@@ -538,7 +574,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         p, r, ncol0 + ch * 32, e, row, valid, rs, inv_out);
                     if (EPI == kSwiglu) {
                         sfbytes |= code << (8 * (ch & 3));
-                        if ((ch & 3) == 3) {
+                        if ((ch & 3) == 3 && mb_in_group) {
                             store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow,
                                            ncol0 + (ch - 3) * 32, valid ? sfbytes : 0u, 4);
                             sfbytes = 0;
@@ -546,7 +582,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            if (EPI == kSwiglu && (C::ACC_BUFS == 1 || C::CHUNKS_W < 4)) {
+            if (EPI == kSwiglu && (C::ACC_BUFS == 1 || C::CHUNKS_W < 4) && mb_in_group) {
                 const int nblk = C::CHUNKS_W < 4 ? C::CHUNKS_W : 4;
                 store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow, ncol0,
                                valid ? sfbytes : 0u, nblk);
@@ -556,6 +592,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // no CTA leaves while its peer may still multicast into it
+    if (C::CM > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -610,9 +648,10 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1>
+template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1,
+          int CM = 1>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, CM>;
     const int64_t kbytes = KIND == kNvfp4 ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
@@ -622,7 +661,7 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     cuuint64_t db[3] = {(cuuint64_t)kbytes, (cuuint64_t)a.N, (cuuint64_t)E};
     cuuint64_t sb[2] = {(cuuint64_t)kbytes, (cuuint64_t)(kbytes * a.N)};
     if (!make_map(&tA, a.a, 2, da, sa, C::BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tB, a.b, 3, db, sb, C::BN)) return cudaErrorInvalidValue;
+    if (!make_map(&tB, a.b, 3, db, sb, C::B_ROWS_CTA)) return cudaErrorInvalidValue;
     Params p;
     p.a_offsets = a.groups.row_offsets;
     p.a_sf_offsets = a.groups.scales_offsets;
@@ -644,13 +683,38 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     p.c_sf = a.c_sf;
     p.err = a.err;
     const int64_t nb = (a.N + BN - 1) / BN;
-    const int64_t tiles_ub = (T / C::BM + a.groups.num_groups) * nb;
-    const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
+    // upper bound of the tiles (cluster tiles for CM > 1) the offsets can give
+    const int64_t tiles_ub = (T / (C::BM * CM) + a.groups.num_groups) * nb;
     auto kern = grouped_gemm_kernel<C, KIND, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+    if (CM == 1) {
+        const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
+        kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+        return cudaGetLastError();
+    }
+    // persistent clusters of CM CTAs: as many as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(sm_count() / CM * CM), 1, 1);
+    int max_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorNotSupported;
+    int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
+    cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, tA, tB, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -687,6 +751,9 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 #ifndef MOEQ_SF_WARPS
 #define MOEQ_SF_WARPS 1
 #endif
+#ifndef MOEQ_GEMM_CM
+#define MOEQ_GEMM_CM 1
+#endif
 #ifndef MOEQ_MX8_STAGES
 #define MOEQ_MX8_STAGES 6
 #endif
@@ -695,15 +762,15 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.kind == kFp8Rowwise && a.epi == kBf16) {
         if (a.N >= 256)
             return run_gemm<kFp8Rowwise, kBf16, MOEQ_FP8_BN, MOEQ_FP8_STAGES, 2,
-                            MOEQ_FP8_EPI_WARPS>(a, s);
+                            MOEQ_FP8_EPI_WARPS, 1, MOEQ_GEMM_CM>(a, s);
         return run_gemm<kFp8Rowwise, kBf16, 64, 8, 2, 4>(a, s);
     }
     if (a.kind == kNvfp4 && a.epi == kBf16)
         return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
+                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS, MOEQ_GEMM_CM>(a, s);
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
+                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, MOEQ_GEMM_CM>(a, s);
     if (a.kind == kMxfp8 && a.epi == kBf16)
         return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;

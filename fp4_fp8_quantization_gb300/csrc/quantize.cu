@@ -19,22 +19,80 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 
+// The group description, read either from a per-CTA shared-memory copy
+// (up to kTableCap groups: one coalesced round trip per CTA instead of a
+// chain of dependent global loads per warp) or from global memory.
+constexpr int kTableCap = 512;
+struct GroupTable {
+    uint32_t ro[kTableCap + 1];
+    uint32_t so[kTableCap + 1];
+    int32_t eid[kTableCap];
+    float scale[kTableCap];  // per-group copy of the expert's fp32 scale
+};
+
+struct GroupView {
+    const uint32_t *ro, *so;
+    const int32_t *eid;
+    const float *scale_g;  // per group (shared copy) or null
+    const float *scale_e;  // per expert (global), used when scale_g is null
+    int G, E;
+    int64_t total_rows, scale_rows_total;
+    __device__ __forceinline__ float scale(int g) const {
+        return scale_g ? scale_g[g] : __ldg(scale_e + eid[g]);
+    }
+};
+
+// Every thread of the CTA must call this (it synchronises the CTA).
+__device__ __forceinline__ GroupView load_groups(const GroupArgs &g, const float *scale_e,
+                                                 GroupTable &t) {
+    GroupView v{g.row_offsets, g.scales_offsets, g.expert_ids, nullptr, scale_e,
+                g.num_groups, g.num_experts, g.total_rows, g.scale_rows_total};
+    if (g.num_groups <= kTableCap) {
+        for (int i = threadIdx.x; i <= g.num_groups; i += blockDim.x) {
+            t.ro[i] = __ldg(g.row_offsets + i);
+            if (g.scales_offsets) t.so[i] = __ldg(g.scales_offsets + i);
+            if (i < g.num_groups) {
+                const int e = __ldg(g.expert_ids + i);
+                t.eid[i] = e;
+                t.scale[i] = (scale_e && e >= 0 && e < g.num_experts) ? __ldg(scale_e + e) : 1.0f;
+            }
+        }
+        __syncthreads();
+        v.ro = t.ro;
+        v.so = g.scales_offsets ? t.so : nullptr;
+        v.eid = t.eid;
+        v.scale_g = t.scale;
+    }
+    return v;
+}
+
+// Largest g in [0, G) with offs[g] <= x (offs[0] <= x); plain loads, so the
+// table may live in shared or global memory.
+__device__ __forceinline__ int find_group(const uint32_t *offs, int G, uint32_t x) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offs[mid] <= x) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
 // Checks one group's offsets / expert id; returns true if it can be used.
-__device__ __forceinline__ bool group_ok(const GroupArgs &g, int gi, uint32_t *err,
+__device__ __forceinline__ bool group_ok(const GroupView &g, int gi, uint32_t *err,
                                          bool need_scales) {
-    uint32_t r0 = __ldg(g.row_offsets + gi), r1 = __ldg(g.row_offsets + gi + 1);
-    int e = __ldg(g.expert_ids + gi);
+    const uint32_t r0 = g.ro[gi], r1 = g.ro[gi + 1];
+    const int e = g.eid[gi];
     if (r1 < r0 || (int64_t)r1 > g.total_rows) {
         set_error(err, MOEQ_DEVERR_BAD_OFFSETS);
         return false;
     }
-    if (e < 0 || e >= g.num_experts) {
+    if (e < 0 || e >= g.E) {
         set_error(err, MOEQ_DEVERR_BAD_EXPERT);
         return false;
     }
     if (need_scales) {
-        uint32_t s0 = __ldg(g.scales_offsets + gi), s1 = __ldg(g.scales_offsets + gi + 1);
-        uint32_t need = (r1 - r0 + 127u) & ~127u;
+        const uint32_t s0 = g.so[gi], s1 = g.so[gi + 1];
+        const uint32_t need = (r1 - r0 + 127u) & ~127u;
         if ((s0 & 127u) || s1 < s0 || s1 - s0 < need || (int64_t)s1 > g.scale_rows_total) {
             set_error(err, MOEQ_DEVERR_SCALE_ROWS);
             return false;
@@ -45,12 +103,11 @@ __device__ __forceinline__ bool group_ok(const GroupArgs &g, int gi, uint32_t *e
 
 // Maps logical scale row p to its group: returns g, or -1 when p lies in no
 // group's scale range (or the group is invalid).
-__device__ __forceinline__ int scale_row_group(const GroupArgs &g, uint32_t p, uint32_t *err) {
-    int G = g.num_groups;
-    uint32_t first = __ldg(g.scales_offsets), last = __ldg(g.scales_offsets + G);
-    if (p < first || p >= last) return -1;
-    int gi = upper_bound_minus1(g.scales_offsets, G, p);
-    if (p >= __ldg(g.scales_offsets + gi + 1)) return -1;
+__device__ __forceinline__ int scale_row_group(const GroupView &g, uint32_t p, uint32_t *err) {
+    const int G = g.G;
+    if (p < g.so[0] || p >= g.so[G]) return -1;
+    const int gi = find_group(g.so, G, p);
+    if (p >= g.so[gi + 1]) return -1;
     return group_ok(g, gi, err, true) ? gi : -1;
 }
 
@@ -104,20 +161,22 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ 
                                                    int64_t stride, int64_t K, GroupArgs g,
                                                    uint32_t *__restrict__ amax_bits,
                                                    uint32_t *err, int rows_per_warp) {
+    __shared__ GroupTable table;
+    const GroupView gv = load_groups(g, nullptr, table);
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t row_begin = warp_id * rows_per_warp;
     const int G = g.num_groups;
-    const uint32_t first = __ldg(g.row_offsets), last = __ldg(g.row_offsets + G);
+    const uint32_t first = gv.ro[0], last = gv.ro[G];
     int cur_e = -1;
     uint32_t cur_m = 0;
     for (int64_t i = 0; i < rows_per_warp; ++i) {
         int64_t row = row_begin + i;
         if (row >= g.total_rows) break;
         if (row < first || row >= last) continue;
-        int gi = upper_bound_minus1(g.row_offsets, G, (uint32_t)row);
-        if (row >= __ldg(g.row_offsets + gi + 1) || !group_ok(g, gi, err, false)) continue;
-        int e = __ldg(g.expert_ids + gi);
+        const int gi = find_group(gv.ro, G, (uint32_t)row);
+        if (row >= gv.ro[gi + 1] || !group_ok(gv, gi, err, false)) continue;
+        const int e = gv.eid[gi];
         const uint4 *src = reinterpret_cast<const uint4 *>(in + row * stride);
         uint32_t m = 0;
         const int64_t n16 = K / 8;
@@ -162,91 +221,153 @@ struct QuantParams {
     uint32_t *err;
 };
 
-// fmt: 0 NVFP4, 1 MXFP4, 2 MXFP8.  One warp per logical scale row.
-template <int FMT>
+// 32 bytes (16 bf16) per lane, read once: one 256-bit load.
+__device__ __forceinline__ void ld_stream32(const void *p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+// max |x| over 16 bf16 (bits), as a bf16 bit pattern.
+__device__ __forceinline__ uint32_t bf16_abs_max16(const uint32_t (&w)[8]) {
+    uint32_t m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = w[2 * i] & 0x7FFF7FFFu, b = w[2 * i + 1] & 0x7FFF7FFFu;
+        asm("max.u16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(a), "r"(b));
+    }
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[1]));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m[2]) : "r"(m[2]), "r"(m[3]));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[2]));
+    return max(m[0] & 0xFFFFu, m[0] >> 16);
+}
+
+// fmt: 0 NVFP4, 1 MXFP4, 2 MXFP8.  One warp per logical scale row; in each
+// 512-element step lane i takes elements [16 i, 16 i + 16): a whole NVFP4
+// block, or half of an MX block (lanes 2j, 2j+1 share block j).
+template <int FMT, bool A32>
 __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
+    __shared__ float r_table[kWarpsPerCta][128];
+    __shared__ GroupTable table;
+    const GroupView gv = load_groups(p.g, FMT == 0 ? p.tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
-    const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    const int wid = threadIdx.x >> 5;
+    const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + wid;
     if (prow >= p.g.scale_rows_total) return;
-    const int gi = scale_row_group(p.g, (uint32_t)prow, p.err);
+    const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
     constexpr int V = FMT == 0 ? 16 : 32;
     const int64_t kv_atoms = p.K / V / 4;
-    const uint32_t r0 = __ldg(p.g.row_offsets + gi);
-    const uint32_t rg = __ldg(p.g.row_offsets + gi + 1) - r0;
-    const uint32_t local = (uint32_t)prow - __ldg(p.g.scales_offsets + gi);
+    const uint32_t r0 = gv.ro[gi];
+    const uint32_t rg = gv.ro[gi + 1] - r0;
+    const uint32_t local = (uint32_t)prow - gv.so[gi];
     if (local >= rg) {  // padding row of this group (up to the next multiple of 128)
         if (local < ((rg + 127u) & ~127u)) zero_scale_row(p.scales, prow, kv_atoms, lane);
         return;
     }
     const int64_t row = (int64_t)r0 + local;
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.in + row * p.stride);
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + row * p.stride);
     float inv = 0.0f;
-    if (FMT == 0) inv = __fdiv_rn(1.0f, __ldg(p.tensor_scale + __ldg(p.g.expert_ids + gi)));
-    // 256 elements per warp step; with K % 256 == 128 the last step has
-    // only lanes 0..15 active (they still take part in the shuffles).
-    const int nchunks = (int)((p.K + 255) / 256);
-    const int lanes_last = (int)((p.K / 8) - (int64_t)(nchunks - 1) * 32);
-    constexpr int U = 8;  // 8 x 16 bytes in flight per lane
-    for (int c0 = 0; c0 < nchunks; c0 += U) {
-        uint4 v[U];
+    if (FMT == 0) {
+        // r depends only on the block's E4M3 scale code: tabulate
+        // r[c] = inv / value(c) once per row (same IEEE division per entry).
+        inv = __fdiv_rn(1.0f, gv.scale(gi));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t c = (uint32_t)(lane * 4 + j);
+            const float sb = e4m3_pos_value(c);
+            r_table[wid][c] = (c == 0 || c >= 0x7F) ? 0.0f : __fdiv_rn(inv, sb);
+        }
+        __syncwarp();
+    }
+    const int nsteps = (int)((p.K + 511) / 512);
+    const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
+    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
+    for (int s0 = 0; s0 < nsteps; s0 += U) {
+        uint32_t w[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (c0 + u < nchunks && (c0 + u < nchunks - 1 || lane < lanes_last))
-                v[u] = ld_stream(src + (int64_t)(c0 + u) * 32 + lane);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            const int s = s0 + u;
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last)) {
+                const uint8_t *a = src + (int64_t)s * 1024 + lane * 32;
+                if (A32) {  // row starts are 32-byte aligned: one 256-bit load
+                    ld_stream32(a, w[u]);
+                } else {
+                    const uint4 lo = ld_stream(a), hi = ld_stream(a + 16);
+                    w[u][0] = lo.x; w[u][1] = lo.y; w[u][2] = lo.z; w[u][3] = lo.w;
+                    w[u][4] = hi.x; w[u][5] = hi.y; w[u][6] = hi.z; w[u][7] = hi.w;
+                }
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int c = c0 + u;
-            if (c >= nchunks) break;
-            const bool active = c < nchunks - 1 || lane < lanes_last;
-            float x[8];
-            bf16x8_to_f32(v[u], x);
-            uint32_t mb = bf16_abs_max8(v[u]);
+            const int s = s0 + u;
+            if (s >= nsteps) break;
+            const bool active = s < nsteps - 1 || lane < lanes_last;
+            uint32_t mb = bf16_abs_max16(w[u]);
             if (FMT == 0) {
-                // block = 16 elements = lanes (2i, 2i+1)
-                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-                Nvfp4Scale s = nvfp4_block_scale(bf16_bits_to_f32(mb), inv);
-                uint32_t codes = nvfp4_codes8(x, s.r);
-                uint32_t word = gather4(s.code, lane, 2);
+                const Nvfp4Scale sc0 = nvfp4_block_scale_code(bf16_bits_to_f32(mb), inv);
+                const float r = r_table[wid][sc0.code];
+                float x[8];
+                uint32_t codes[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[2 * i] = bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu);
+                        x[2 * i + 1] = __uint_as_float(w[u][4 * h + i] & 0xFFFF0000u);
+                    }
+                    codes[h] = nvfp4_codes8(x, r);
+                }
+                const uint32_t word = gather4(sc0.code, lane, 1);
                 if (!active) continue;
-                reinterpret_cast<uint32_t *>(p.out + row * (p.K / 2))[c * 32 + lane] = codes;
-                if ((lane & 7) == 0)
+                reinterpret_cast<uint2 *>(p.out + row * (p.K / 2))[s * 32 + lane] =
+                    make_uint2(codes[0], codes[1]);
+                if ((lane & 3) == 0)
                     *reinterpret_cast<uint32_t *>(
-                        p.scales + sf_word_offset(prow, c * 4 + (lane >> 3), kv_atoms)) = word;
+                        p.scales + sf_word_offset(prow, s * 8 + (lane >> 2), kv_atoms)) = word;
             } else {
-                // block = 32 elements = lanes (4i .. 4i+3)
-                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));  // block = lanes 2j, 2j+1
                 constexpr int emax = FMT == 2 ? 8 : 2;
                 uint32_t code = 0;
-                float y[8];
-                if (mb == 0) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = 0.0f;
-                } else {
+                float f = 0.0f;
+                if (mb != 0) {
                     int cs = bf16_floor_log2(mb) - emax + 127;
                     cs = min(max(cs, 0), 254);
                     code = (uint32_t)cs;
-                    float f = __uint_as_float((uint32_t)(254 - cs) << 23);  // 2^(127-c)
+                    f = __uint_as_float((uint32_t)(254 - cs) << 23);  // 2^(127-c)
+                }
+                uint32_t o[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[i], f);
+                for (int h = 0; h < 2; ++h) {
+                    float y[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        y[2 * i] = __fmul_rn(bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu), f);
+                        y[2 * i + 1] = __fmul_rn(__uint_as_float(w[u][4 * h + i] & 0xFFFF0000u), f);
+                    }
+                    if (FMT == 2) {
+                        o[2 * h] = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+                        o[2 * h + 1] = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
+                    } else {
+                        o[h] = e2m1x8(y);
+                    }
                 }
-                uint32_t word = gather4(code, lane, 4);
+                if (mb == 0) o[0] = o[1] = o[2] = o[3] = 0u;  // all-zero block: +0 codes
+                const uint32_t word = gather4(code, lane, 2);
                 if (!active) continue;
-                if (FMT == 2) {
-                    uint32_t lo = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
-                    uint32_t hi = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
-                    if (mb == 0) lo = hi = 0u;
-                    reinterpret_cast<uint2 *>(p.out + row * p.K)[c * 32 + lane] = make_uint2(lo, hi);
-                } else {
-                    uint32_t codes = (mb == 0) ? 0u : e2m1x8(y);
-                    reinterpret_cast<uint32_t *>(p.out + row * (p.K / 2))[c * 32 + lane] = codes;
-                }
-                if ((lane & 15) == 0)
+                if (FMT == 2)
+                    st_global_v4(p.out + row * p.K + (int64_t)s * 512 + lane * 16, o[0], o[1], o[2],
+                                 o[3]);
+                else
+                    reinterpret_cast<uint2 *>(p.out + row * (p.K / 2))[s * 32 + lane] =
+                        make_uint2(o[0], o[1]);
+                if ((lane & 7) == 0)
                     *reinterpret_cast<uint32_t *>(
-                        p.scales + sf_word_offset(prow, c * 2 + (lane >> 4), kv_atoms)) = word;
+                        p.scales + sf_word_offset(prow, s * 4 + (lane >> 3), kv_atoms)) = word;
             }
         }
     }
@@ -267,21 +388,23 @@ struct SwigluParams {
 // One warp per logical scale row; a lane takes 8 (gate, up) pairs = 8 h
 // values per 256-h step, so a 16-h block is held by lanes (2i, 2i+1).
 __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
+    __shared__ GroupTable table;
+    const GroupView gv = load_groups(p.g, p.out_tensor_scale, table);
     const int lane = threadIdx.x & 31;
     const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (prow >= p.g.scale_rows_total) return;
-    const int gi = scale_row_group(p.g, (uint32_t)prow, p.err);
+    const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
     const int64_t kv_atoms = p.I / 64;
-    const uint32_t r0 = __ldg(p.g.row_offsets + gi);
-    const uint32_t rg = __ldg(p.g.row_offsets + gi + 1) - r0;
-    const uint32_t local = (uint32_t)prow - __ldg(p.g.scales_offsets + gi);
+    const uint32_t r0 = gv.ro[gi];
+    const uint32_t rg = gv.ro[gi + 1] - r0;
+    const uint32_t local = (uint32_t)prow - gv.so[gi];
     if (local >= rg) {
         if (local < ((rg + 127u) & ~127u)) zero_scale_row(p.scales, prow, kv_atoms, lane);
         return;
     }
     const int64_t row = (int64_t)r0 + local;
-    const float inv = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + __ldg(p.g.expert_ids + gi)));
+    const float inv = __fdiv_rn(1.0f, gv.scale(gi));
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;
     constexpr int U = 3;  // 256-h steps whose loads are issued together
@@ -365,7 +488,8 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
     cudaError_t e = cudaMemsetAsync(tensor_scale_out, 0, sizeof(float) * g.num_experts, s);
     if (e != cudaSuccess) return e;
     if (g.total_rows > 0) {
-        const int rows_per_warp = 4;
+        // enough warps to fill the GPU on small inputs, 4 rows each on large
+        const int rows_per_warp = g.total_rows >= 65536 ? 4 : 1;
         int64_t warps = (g.total_rows + rows_per_warp - 1) / rows_per_warp;
         int64_t blocks = (warps + 7) / 8;
         amax_kernel<<<(unsigned)blocks, 256, 0, s>>>(
@@ -384,12 +508,17 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
                   g, err};
     int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks == 0) return cudaSuccess;
+    // 256-bit loads need every row start 32-byte aligned
+    const bool a32 = (reinterpret_cast<uintptr_t>(in) % 32 == 0) && (stride % 16 == 0);
     if (fmt == 0)
-        quantize_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<0, true><<<(unsigned)blocks, 256, 0, s>>>(p)
+            : quantize_kernel<0, false><<<(unsigned)blocks, 256, 0, s>>>(p);
     else if (fmt == 1)
-        quantize_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<1, true><<<(unsigned)blocks, 256, 0, s>>>(p)
+            : quantize_kernel<1, false><<<(unsigned)blocks, 256, 0, s>>>(p);
     else
-        quantize_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<2, true><<<(unsigned)blocks, 256, 0, s>>>(p)
+            : quantize_kernel<2, false><<<(unsigned)blocks, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

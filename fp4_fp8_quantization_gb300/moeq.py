@@ -88,6 +88,18 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def _ptr_rows(t, dtype, name):
+    """Pointer of a 2-D tensor whose rows may be strided (unit element
+    stride, row stride >= row length)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.dim() != 2 or t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name}: must be 2-D with unit column stride")
+    return t.data_ptr()
+
+
 def _call(fn, *args):
     st = getattr(lib(), fn)(*args)
     if st != 0:
@@ -105,7 +117,7 @@ _U32 = (torch.uint32, torch.int32)
 def grouped_amax_scale(inp, row_offsets, expert_ids, tensor_scale_out, num_experts,
                        num_active_experts=None, stream=None):
     G = expert_ids.numel() if num_active_experts is None else num_active_experts
-    _call("moeq_grouped_amax_scale", _ptr(inp, torch.bfloat16, "inp"), inp.stride(0),
+    _call("moeq_grouped_amax_scale", _ptr_rows(inp, torch.bfloat16, "inp"), inp.stride(0),
           inp.shape[0], inp.shape[1], _ptr(row_offsets, _U32), _ptr(expert_ids, torch.int32),
           _ptr(tensor_scale_out, torch.float32), num_experts, G, _stream(stream))
 
@@ -114,7 +126,7 @@ def grouped_quantize(fmt, inp, out, scales, row_offsets, scales_offsets, expert_
                      tensor_scale, num_experts, scale_rows_total, max_tokens_per_expert=0,
                      num_active_experts=None, stream=None):
     G = expert_ids.numel() if num_active_experts is None else num_active_experts
-    _call("moeq_grouped_quantize", _fmt(fmt), _ptr(inp, torch.bfloat16, "inp"), inp.stride(0),
+    _call("moeq_grouped_quantize", _fmt(fmt), _ptr_rows(inp, torch.bfloat16, "inp"), inp.stride(0),
           inp.shape[0], inp.shape[1], _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"),
           scale_rows_total, _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32),
           _ptr(expert_ids, torch.int32), _ptr(tensor_scale, torch.float32), num_experts,

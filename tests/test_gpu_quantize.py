@@ -104,6 +104,38 @@ def test_quantize_special_values(fmt):
     assert np.array_equal(sf, want_sf)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_strided_rows(fmt):
+    """Rows 16- but not 32-byte aligned (row stride K + 8 elements, and a
+    view starting 8 elements in): the kernel's two-16-byte-load path."""
+    need_gpu()
+    counts = [3, 130, 0, 40]
+    ro, ids = groups_from_counts(counts, [1, 0, 3, 2])
+    so = Q.padded_scale_offsets(ro)
+    T, K, E = int(ro[-1]), 256, 4
+    rows = int(so[-1])
+    base = synth.bf16_normal((T, K + 16), 1.0, seed=8)
+    view = base[:, 8:8 + K]
+    x_np = view.float().numpy()
+    ts = _oracle_ts(x_np, ro, ids, E)
+    dev_base = base.to(DEV)
+    x_dev = dev_base[:, 8:8 + K]
+    assert x_dev.stride(0) == K + 16 and (x_dev.data_ptr() % 32) != 0
+    ob = K if fmt == "mxfp8" else K // 2
+    out = torch.full((T, ob), 0xA5, dtype=torch.uint8, device=DEV)
+    sf = torch.full((moeq.sf_bytes(rows, K // _v(fmt)),), 0x5A, dtype=torch.uint8, device=DEV)
+    moeq.grouped_quantize(fmt, x_dev, out, sf, to_dev_u32(ro), to_dev_u32(so), to_dev_i32(ids),
+                          torch.from_numpy(ts).to(DEV), E, rows)
+    want_out, want_sf = Q.grouped_quantize(fmt, x_np, ro, so, ids, ts,
+                                           out=np.full((T, ob), 0xA5, np.uint8),
+                                           scales=np.full(L.physical_bytes(rows, K // _v(fmt)), 0x5A,
+                                                          np.uint8), scale_rows_total=rows)
+    assert np.array_equal(u8(out), want_out) and np.array_equal(u8(sf), want_sf)
+    amax = torch.empty(E, device=DEV)
+    moeq.grouped_amax_scale(x_dev, to_dev_u32(ro), to_dev_i32(ids), amax, E)
+    assert np.array_equal(amax.cpu().numpy().view(np.uint32), ts.view(np.uint32))
+
+
 def _cfg2(seed=0):
     counts = synth.routing_counts(4096, 2, 8, seed=seed)
     ro, ids = synth.ragged_groups(counts)
