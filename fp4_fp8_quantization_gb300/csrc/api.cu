@@ -192,11 +192,10 @@ static moeq_status blockscaled_common(moeq_format fmt, int epi, const uint8_t *a
     if (!groups_ok(a_offsets, expert_ids, num_experts, num_active_experts))
         return MOEQ_ERR_INVALID_ARG;
     if (fmt != MOEQ_NVFP4 && fmt != MOEQ_MXFP4 && fmt != MOEQ_MXFP8) return MOEQ_ERR_INVALID_ARG;
-    if (fmt == MOEQ_MXFP4) return MOEQ_ERR_UNSUPPORTED;
     if (total_tokens < 0 || N <= 0 || K <= 0 || N % 128 || scale_rows_total < 0 ||
         scale_rows_total % 128)
         return MOEQ_ERR_INVALID_ARG;
-    if (fmt == MOEQ_NVFP4 ? (K % 256) : (K % 128)) return MOEQ_ERR_INVALID_ARG;
+    if (fmt == MOEQ_MXFP8 ? (K % 128) : (K % 256)) return MOEQ_ERR_INVALID_ARG;
     if (total_tokens >= (int64_t)1 << 31 || N >= (int64_t)1 << 31 || K >= (int64_t)1 << 31)
         return MOEQ_ERR_UNSUPPORTED;
     if (num_active_experts > moeq::kMaxGroups) return MOEQ_ERR_UNSUPPORTED;
@@ -206,7 +205,7 @@ static moeq_status blockscaled_common(moeq_format fmt, int epi, const uint8_t *a
         (!a || !a_sf || !aligned16(a) || !aligned16(a_sf)))
         return MOEQ_ERR_INVALID_ARG;
     *ga = moeq::GemmArgs{};
-    ga->kind = fmt == MOEQ_NVFP4 ? 1 : 2;
+    ga->kind = fmt == MOEQ_NVFP4 ? 1 : (fmt == MOEQ_MXFP8 ? 2 : 3);
     ga->epi = epi;
     ga->groups = make_groups(a_offsets, a_scales_offsets, expert_ids, num_active_experts,
                              num_experts, total_tokens, scale_rows_total);

@@ -393,6 +393,24 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int sf_id) 
            ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
 }
 
+// kind::mxf4, E2M1 x E2M1 with UE8M0 scales (32-element blocks); sf_id 0 or
+// 2 picks the byte pair of the scale cell (two blocks per K=64 step).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                            uint32_t accumulate) {
     asm volatile(

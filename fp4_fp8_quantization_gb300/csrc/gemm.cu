@@ -1,5 +1,5 @@
 // Grouped (ragged mixture-of-experts) GEMMs on the 5th-generation tensor
-// cores: FP8 rowwise-scaled, NVFP4 and MXFP8 block-scaled, with a bf16
+// cores: FP8 rowwise-scaled, NVFP4 / MXFP4 / MXFP8 block-scaled, with a bf16
 // epilogue or the fused SwiGLU + NVFP4 requantization epilogue.
 //
 // Pages: "grouped_matmul_rowwise_dynamic_scaled_fp8" (the rowwise formula,
@@ -18,14 +18,23 @@
 //    and B tiles (BN rows x 128 bytes) land 128B-swizzled in a STAGES-deep
 //    shared-memory ring; block-scaled kinds also bulk-copy the 512-byte
 //    scale atoms of the k-tile (contiguous in the tiled scale layout).
-//  * warp 1 (one thread): tcgen05.mma issuer.  Scale atoms go shared ->
-//    TMEM with tcgen05.cp (one TMEM slot per ring stage), the MMAs
-//    accumulate in one of two TMEM accumulators (double buffered, so the
-//    epilogue of tile i overlaps the mainloop of tile i+1), tcgen05.commit
-//    frees ring stages and publishes finished accumulators.
-//  * warps 2..5: epilogue.  Each warp owns a 32-lane quarter of TMEM (one
-//    row per thread), reads 32 fp32 columns at a time with tcgen05.ld and
-//    applies the scales (and SwiGLU + NVFP4 requant) in registers.
+//  * warp 1 (one thread): tcgen05.mma issuer.  The MMAs accumulate in TMEM
+//    (FP8: two 128x256 accumulators, so the epilogue of tile i overlaps the
+//    mainloop of tile i+1; block-scaled: one 128x256 accumulator, because
+//    the per-stage scale slots take the rest of TMEM); tcgen05.commit frees
+//    ring stages and publishes finished accumulators.
+//  * block-scaled kinds: warp 2 (one thread) moves each stage's scale atoms
+//    shared -> TMEM with tcgen05.cp into that stage's TMEM slot and signals
+//    the MMA thread through a per-stage barrier, so the MMA thread issues
+//    only MMAs.
+//  * remaining warps: epilogue.  Each warp owns a 32-lane quarter of TMEM
+//    (one row per thread) and a column range; it reads 32 fp32 columns per
+//    tcgen05.ld, frees the accumulator as soon as its columns are in
+//    registers (single-accumulator kinds), then applies the scales (and
+//    SwiGLU + NVFP4 requant) in registers.
+//  * optional (compile-time, off by default): clusters of two CTAs on
+//    consecutive m-blocks of one expert, each loading half of every B tile
+//    and multicasting it to both.
 //  * every wait is bounded (about one second) and sets the device error
 //    word instead of hanging.
 #include "common.cuh"
@@ -35,7 +44,7 @@ namespace moeq {
 
 namespace {
 
-enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2 };
+enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2, kMxfp4 = 3 };
 enum Epi { kBf16 = 0, kSwiglu = 1 };
 
 template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
@@ -47,7 +56,7 @@ struct Cfg {
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;                  // TMEM accumulators
     static constexpr int BK_BYTES = 128;                        // one 128B swizzle row
-    static constexpr int ELEMS_PER_BYTE = KIND == kNvfp4 ? 2 : 1;
+    static constexpr int ELEMS_PER_BYTE = (KIND == kNvfp4 || KIND == kMxfp4) ? 2 : 1;
     static constexpr int BK = BK_BYTES * ELEMS_PER_BYTE;        // K elements per stage
     static constexpr int KSTEPS = 4;                            // 32 bytes of K per MMA
     static constexpr bool SCALED = KIND != kFp8Rowwise;
@@ -435,6 +444,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         } else if (KIND == kNvfp4) {
                             mma_nvf4(d, ad, bd, idesc_nvf4(C::BM, C::BN), tsfa + 4 * ks,
                                      tsfb + 4 * C::RB * ks, acc);
+                        } else if (KIND == kMxfp4) {
+                            // scale atom ks / 2 holds 4 blocks of 32 = two K=64 steps
+                            mma_mxf4(d, ad, bd, idesc_mxf4(C::BM, C::BN, (ks & 1) * 2),
+                                     tsfa + 4 * (ks >> 1), tsfb + 4 * C::RB * (ks >> 1), acc);
                         } else {
                             mma_mxf8(d, ad, bd, idesc_mxf8_e4m3(C::BM, C::BN, ks), tsfa, tsfb,
                                      acc);
@@ -652,7 +665,7 @@ template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, in
           int CM = 1>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, CM>;
-    const int64_t kbytes = KIND == kNvfp4 ? a.K / 2 : a.K;
+    const int64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
     CUtensorMap tA, tB;
@@ -771,6 +784,9 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
                         MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, MOEQ_GEMM_CM>(a, s);
+    if (a.kind == kMxfp4 && a.epi == kBf16)
+        return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
+                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
     if (a.kind == kMxfp8 && a.epi == kBf16)
         return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;

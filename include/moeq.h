@@ -160,15 +160,14 @@ moeq_status moeq_grouped_matmul_rowwise_fp8(
  * block-scaled matmul with per-expert scales"; expert_scales are the
  * "per-expert matmul-epilogue scaling factors"):
  *   c[t, n] = bf16( expert_scales[e] * sum_k (qa[t,k] * sa[t,k/v]) * (qb[e,n,k] * sb[e,n,k/v]) )
- * with e = expert_ids[g], v = 16 (NVFP4) or 32 (MXFP8).
- *   a      NVFP4: packed [total_tokens, K/2]; MXFP8: [total_tokens, K]
+ * with e = expert_ids[g], v = 16 (NVFP4) or 32 (MXFP8, MXFP4).
+ *   a      NVFP4 / MXFP4: packed [total_tokens, K/2]; MXFP8: [total_tokens, K]
  *   a_sf   tiled scales, scale_rows_total rows; row t of group g uses
  *          scale row a_scales_offsets[g] + (t - a_offsets[g])
- *   b      NVFP4: packed [num_experts, N, K/2]; MXFP8: [num_experts, N, K]
+ *   b      NVFP4 / MXFP4: packed [num_experts, N, K/2]; MXFP8: [num_experts, N, K]
  *   b_sf   per-expert tiled scales (see the layout above)
  *   expert_scales  fp32 [num_experts]; required for NVFP4, NULL means 1 for MX.
- * NVFP4: K % 256 == 0; MXFP8: K % 128 == 0; N % 128 == 0.  MXFP4 returns
- * MOEQ_ERR_UNSUPPORTED. */
+ * NVFP4 and MXFP4: K % 256 == 0; MXFP8: K % 128 == 0; N % 128 == 0. */
 moeq_status moeq_grouped_matmul_blockscaled(
     moeq_format fmt, void *c, const uint8_t *a, const uint8_t *a_sf,
     const uint8_t *b, const uint8_t *b_sf, const float *expert_scales,

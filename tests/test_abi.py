@@ -77,8 +77,10 @@ def test_gemms_reject_bad_host_arguments(lib):
     assert r(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 128, 2, 8, 0, None) == 0
     bs = lib.moeq_grouped_matmul_blockscaled
     args = [0] + [FAKE] * 9 + [64, 128, 128, 512, 2, 8, 2, None]
-    a = list(args); a[0] = 1                                 # MXFP4 GEMM: not built
-    assert bs(*a) == 2
+    a = list(args); a[0] = 1; a[13] = 384                    # MXFP4 needs K % 256
+    assert bs(*a) == 1
+    a = list(args); a[0] = 7                                 # unknown format
+    assert bs(*a) == 1
     a = list(args); a[0] = 0; a[6] = None                    # NVFP4 without expert scales
     assert bs(*a) == 1
     a = list(args); a[0] = 0; a[13] = 384                    # NVFP4 needs K % 256

@@ -171,6 +171,11 @@ def blockscaled_inputs(fmt, T, E, N, K, rows, seed, device="cpu", a_sf=(0x20, 0x
         kv = K // 16
         lo_a, hi_a = a_sf
         lo_b, hi_b = b_sf
+    elif fmt == "mxfp4":
+        a = synth.random_fp4_packed((T, K // 2), seed=seed, device=device)
+        b = synth.random_fp4_packed((E, N, K // 2), seed=seed + 1, device=device)
+        kv = K // 32
+        lo_a, hi_a, lo_b, hi_b = 118, 130, 116, 126
     else:
         a = synth.e4m3_normal((T, K), 1.0, seed=seed, device=device).view(torch.uint8)
         b = synth.e4m3_normal((E, N, K), 1.0, seed=seed + 1, device=device).view(torch.uint8)
@@ -192,7 +197,8 @@ def run_blockscaled(fmt, a, asf, b, bsf, es, ro, so, ids, N, K, rows):
     return c
 
 
-@pytest.mark.parametrize("fmt,es_on", [("nvfp4", True), ("mxfp8", False), ("mxfp8", True)])
+@pytest.mark.parametrize("fmt,es_on", [("nvfp4", True), ("mxfp8", False), ("mxfp8", True),
+                                       ("mxfp4", False), ("mxfp4", True)])
 @pytest.mark.parametrize("N,K", [(256, 512), (128, 1024)])
 def test_blockscaled_ragged_multitile(fmt, es_on, N, K):
     need_gpu()
@@ -278,3 +284,28 @@ def test_mxfp8_decode_shape_sampled():
             None, np.array([0, r1 - r0], np.uint32), np.array([0, 128], np.uint32), [0],
             N=N, K=K, scale_rows_total=128, return_f64=True)
         assert_gemm_close(c[r0:r1], f64)
+
+
+def test_mxfp4_blockscaled_moe_scale_sampled():
+    """MXFP4 at the 128-expert shape (K = 4096, N = 3072), sampled rows."""
+    need_gpu()
+    from oracle import layout as L
+    counts, ro, ids, so = _cfg4_groups(seed=1)
+    T, E, N, K = int(ro[-1]), 128, 3072, 4096
+    rows = int(so[-1])
+    a, asf, b, bsf, _ = blockscaled_inputs("mxfp4", T, E, N, K, rows, seed=45, device=DEV)
+    c = bf16_bits(run_blockscaled("mxfp4", a, asf, b, bsf, None, ro, so, ids, N, K, rows))
+    kv = K // 32
+    per = moeq.sf_bytes(N, kv)
+    a_np, bsf_np = u8(a), u8(bsf)
+    lg = L.unswizzle(u8(asf), rows, kv)
+    for g in np.linspace(0, len(ids) - 1, 12).astype(int):
+        e, r0 = int(ids[g]), int(ro[g])
+        rr = np.arange(r0, min(r0 + 3, int(ro[g + 1])))
+        pad = np.zeros((128, kv), np.uint8)
+        pad[:len(rr)] = lg[int(so[g]) + rr - r0]
+        _, f64 = OG.grouped_matmul_blockscaled(
+            "mxfp4", a_np[rr], L.swizzle(pad), u8(b[e:e + 1]), bsf_np[e * per:(e + 1) * per], None,
+            np.array([0, len(rr)], np.uint32), np.array([0, 128], np.uint32), [0], N=N, K=K,
+            scale_rows_total=128, return_f64=True)
+        assert_gemm_close(c[rr], f64)
