@@ -336,6 +336,35 @@ def chained_part(d, pk):
             "chained_total_ms": round(t_g + t_s, 4), "fused_bytes_equal_chained": same}
 
 
+def layer_part(d):
+    """Whole MoE FFN expert layer on the same batch: the up-projection step
+    followed by the NVFP4 down-projection GEMM (K = I = 1536, N = 4096) on the
+    fused kernel's packed output and its padded scales."""
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    H = K4
+    bd = synth.random_fp4_packed((E4, H, I4 // 2), seed=90, device="cuda")
+    bdsf = synth.random_bytes(E4 * moeq.sf_bytes(H, I4 // 16), 0x18, 0x28, seed=91, device="cuda")
+    esd = synth.uniform((E4,), 0.5, 2.0, seed=92, device="cuda")
+    out = torch.empty((d["T"], H), dtype=torch.bfloat16, device="cuda")
+
+    def down():
+        moeq.grouped_matmul_blockscaled("nvfp4", out, d["c"], d["csf"], bd, bdsf, esd, d["ro"],
+                                        d["so"], d["ids"], H, I4, d["rows"], d["mt"])
+
+    def layer():
+        up_projection_step(d)
+        down()
+
+    t_down = time_kernel(down, 10)
+    t_layer = time_kernel(layer, 10)
+    fl = flops_up(d) + 2.0 * d["T"] * H * I4
+    return {"down_proj_ms": round(t_down, 4),
+            "down_proj_TFLOP/s": round(2.0 * d["T"] * H * I4 / t_down / 1e9, 1),
+            "layer_ms": round(t_layer, 4), "layer_TFLOP/s": round(fl / t_layer / 1e9, 1),
+            "layer": "amax -> NVFP4 quantize -> fused gate/up GEMM + SwiGLU + requant -> "
+                     "NVFP4 down-projection GEMM (bf16 out)"}
+
+
 # --------------------------------------------------------- CPU baseline
 
 def cpu_oracle_sample(d, groups, max_rows=None):
@@ -490,6 +519,7 @@ def run_moeq(args, rank, world):
     extra = {}
     if rank == 0 and not args.no_parts:
         extra["chained_same_workload"] = chained_part(d, pk)
+        extra["moe_layer_same_workload"] = layer_part(d)
         extra.update(parts(pk, None))
     err = moeq.get_device_error()
 

@@ -98,11 +98,11 @@ moeq_status moeq_padded_scale_offsets(const uint32_t *row_offsets, uint32_t *sca
         moeq::launch_padded_offsets(row_offsets, scales_offsets, num_active_experts, stream));
 }
 
-moeq_status moeq_grouped_amax_scale(const void *in, int64_t in_row_stride, int64_t total_rows,
-                                    int64_t K, const uint32_t *row_offsets,
-                                    const int32_t *expert_ids, float *tensor_scale_out,
-                                    int32_t num_experts, int32_t num_active_experts,
-                                    moeq_stream_t stream) {
+static moeq_status amax_impl(const void *in, int64_t in_row_stride, int64_t total_rows,
+                             int64_t K, const uint32_t *row_offsets, const int32_t *expert_ids,
+                             float *tensor_scale_out, int32_t num_experts,
+                             int32_t num_active_experts, const moeq::Gather &gt,
+                             moeq_stream_t stream) {
     if (!groups_ok(row_offsets, expert_ids, num_experts, num_active_experts))
         return MOEQ_ERR_INVALID_ARG;
     if (!tensor_scale_out || total_rows < 0 || K <= 0 || K % 8 || in_row_stride < K ||
@@ -115,17 +115,16 @@ moeq_status moeq_grouped_amax_scale(const void *in, int64_t in_row_stride, int64
     moeq::GroupArgs g = make_groups(row_offsets, nullptr, expert_ids, num_active_experts,
                                     num_experts, num_active_experts ? total_rows : 0, 0);
     return cuda_status(
-        moeq::launch_amax_scale(in, in_row_stride, K, g, tensor_scale_out, err, stream));
+        moeq::launch_amax_scale(in, in_row_stride, K, g, gt, tensor_scale_out, err, stream));
 }
 
-moeq_status moeq_grouped_quantize(moeq_format fmt, const void *in, int64_t in_row_stride,
-                                  int64_t total_rows, int64_t K, uint8_t *out, uint8_t *scales,
-                                  int64_t scale_rows_total, const uint32_t *row_offsets,
-                                  const uint32_t *scales_offsets, const int32_t *expert_ids,
-                                  const float *tensor_scale, int32_t num_experts,
-                                  int32_t max_tokens_per_expert, int32_t num_active_experts,
-                                  moeq_stream_t stream) {
-    (void)max_tokens_per_expert;
+static moeq_status quantize_impl(moeq_format fmt, const void *in, int64_t in_row_stride,
+                                 int64_t total_rows, int64_t K, uint8_t *out, uint8_t *scales,
+                                 int64_t scale_rows_total, const uint32_t *row_offsets,
+                                 const uint32_t *scales_offsets, const int32_t *expert_ids,
+                                 const float *tensor_scale, int32_t num_experts,
+                                 int32_t num_active_experts, const moeq::Gather &gt,
+                                 moeq_stream_t stream) {
     if (fmt != MOEQ_NVFP4 && fmt != MOEQ_MXFP4 && fmt != MOEQ_MXFP8) return MOEQ_ERR_INVALID_ARG;
     if (!groups_ok(row_offsets, expert_ids, num_experts, num_active_experts))
         return MOEQ_ERR_INVALID_ARG;
@@ -142,7 +141,68 @@ moeq_status moeq_grouped_quantize(moeq_format fmt, const void *in, int64_t in_ro
     moeq::GroupArgs g = make_groups(row_offsets, scales_offsets, expert_ids, num_active_experts,
                                     num_experts, total_rows, scale_rows_total);
     return cuda_status(moeq::launch_quantize((int)fmt, in, in_row_stride, K, out, scales,
-                                             tensor_scale, g, err, stream));
+                                             tensor_scale, g, gt, err, stream));
+}
+
+static bool gather_ok(const int32_t *indices, int32_t indices_divisor, int64_t in_rows,
+                      int64_t total_rows) {
+    return indices_divisor >= 1 && in_rows >= 0 && (total_rows == 0 || indices);
+}
+
+moeq_status moeq_grouped_amax_scale(const void *in, int64_t in_row_stride, int64_t total_rows,
+                                    int64_t K, const uint32_t *row_offsets,
+                                    const int32_t *expert_ids, float *tensor_scale_out,
+                                    int32_t num_experts, int32_t num_active_experts,
+                                    moeq_stream_t stream) {
+    const moeq::Gather none{nullptr, 1, total_rows};
+    return amax_impl(in, in_row_stride, total_rows, K, row_offsets, expert_ids, tensor_scale_out,
+                     num_experts, num_active_experts, none, stream);
+}
+
+moeq_status moeq_grouped_amax_scale_gather(const void *in, int64_t in_row_stride,
+                                           int64_t in_rows, int64_t K,
+                                           const int32_t *indices, int32_t indices_divisor,
+                                           int64_t total_rows, const uint32_t *row_offsets,
+                                           const int32_t *expert_ids, float *tensor_scale_out,
+                                           int32_t num_experts, int32_t num_active_experts,
+                                           moeq_stream_t stream) {
+    if (!gather_ok(indices, indices_divisor, in_rows, total_rows)) return MOEQ_ERR_INVALID_ARG;
+    if (in_rows == 0 && total_rows > 0 && num_active_experts > 0) return MOEQ_ERR_INVALID_ARG;
+    const moeq::Gather gt{indices, indices_divisor, in_rows};
+    return amax_impl(in, in_row_stride, total_rows, K, row_offsets, expert_ids, tensor_scale_out,
+                     num_experts, num_active_experts, gt, stream);
+}
+
+moeq_status moeq_grouped_quantize(moeq_format fmt, const void *in, int64_t in_row_stride,
+                                  int64_t total_rows, int64_t K, uint8_t *out, uint8_t *scales,
+                                  int64_t scale_rows_total, const uint32_t *row_offsets,
+                                  const uint32_t *scales_offsets, const int32_t *expert_ids,
+                                  const float *tensor_scale, int32_t num_experts,
+                                  int32_t max_tokens_per_expert, int32_t num_active_experts,
+                                  moeq_stream_t stream) {
+    (void)max_tokens_per_expert;
+    const moeq::Gather none{nullptr, 1, total_rows};
+    return quantize_impl(fmt, in, in_row_stride, total_rows, K, out, scales, scale_rows_total,
+                         row_offsets, scales_offsets, expert_ids, tensor_scale, num_experts,
+                         num_active_experts, none, stream);
+}
+
+moeq_status moeq_grouped_quantize_gather(moeq_format fmt, const void *in, int64_t in_row_stride,
+                                         int64_t in_rows, int64_t K, const int32_t *indices,
+                                         int32_t indices_divisor, int64_t total_rows,
+                                         uint8_t *out, uint8_t *scales, int64_t scale_rows_total,
+                                         const uint32_t *row_offsets,
+                                         const uint32_t *scales_offsets,
+                                         const int32_t *expert_ids, const float *tensor_scale,
+                                         int32_t num_experts, int32_t max_tokens_per_expert,
+                                         int32_t num_active_experts, moeq_stream_t stream) {
+    (void)max_tokens_per_expert;
+    if (!gather_ok(indices, indices_divisor, in_rows, total_rows)) return MOEQ_ERR_INVALID_ARG;
+    if (in_rows == 0 && total_rows > 0 && num_active_experts > 0) return MOEQ_ERR_INVALID_ARG;
+    const moeq::Gather gt{indices, indices_divisor, in_rows};
+    return quantize_impl(fmt, in, in_row_stride, total_rows, K, out, scales, scale_rows_total,
+                         row_offsets, scales_offsets, expert_ids, tensor_scale, num_experts,
+                         num_active_experts, gt, stream);
 }
 
 moeq_status moeq_grouped_matmul_rowwise_fp8(void *c, const uint8_t *a, const uint8_t *b,

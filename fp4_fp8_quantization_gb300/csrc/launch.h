@@ -18,12 +18,21 @@ struct GroupArgs {
     int64_t scale_rows_total;
 };
 
+// Optional row gather of the streaming kernels: quantized row t reads input
+// row indices[t] / divisor (in_rows input rows); indices == null: row t.
+struct Gather {
+    const int32_t *indices;
+    int32_t divisor;
+    int64_t in_rows;
+};
+
 cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const GroupArgs &g,
-                              float *tensor_scale_out, uint32_t *err, cudaStream_t s);
+                              const Gather &gt, float *tensor_scale_out, uint32_t *err,
+                              cudaStream_t s);
 
 cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,
                             uint8_t *scales, const float *tensor_scale, const GroupArgs &g,
-                            uint32_t *err, cudaStream_t s);
+                            const Gather &gt, uint32_t *err, cudaStream_t s);
 
 cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_offsets,
                                   int32_t num_groups, cudaStream_t s);

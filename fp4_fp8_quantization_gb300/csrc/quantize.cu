@@ -157,8 +157,23 @@ __device__ __forceinline__ void zero_scale_row(uint8_t *scales, int64_t p, int64
 
 // --------------------------------------------------------------- amax pass
 
+// Input row of quantized row `row`: row itself, or indices[row] / divisor
+// when the rows are gathered; -1 (with the error bit set) when the index
+// falls outside the input.
+__device__ __forceinline__ int64_t source_row(const Gather &gt, int64_t row, uint32_t *err) {
+    if (!gt.indices) return row;
+    const int32_t v = __ldg(gt.indices + row);
+    const int64_t s = v < 0 ? -1 : (int64_t)(v / gt.divisor);
+    if (s < 0 || s >= gt.in_rows) {
+        set_error(err, MOEQ_DEVERR_BAD_INDEX);
+        return -1;
+    }
+    return s;
+}
+
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ in,
                                                    int64_t stride, int64_t K, GroupArgs g,
+                                                   Gather gt,
                                                    uint32_t *__restrict__ amax_bits,
                                                    uint32_t *err, int rows_per_warp) {
     __shared__ GroupTable table;
@@ -177,7 +192,9 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ 
         const int gi = find_group(gv.ro, G, (uint32_t)row);
         if (row >= gv.ro[gi + 1] || !group_ok(gv, gi, err, false)) continue;
         const int e = gv.eid[gi];
-        const uint4 *src = reinterpret_cast<const uint4 *>(in + row * stride);
+        const int64_t srow = source_row(gt, row, err);
+        if (srow < 0) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + srow * stride);
         uint32_t m = 0;
         const int64_t n16 = K / 8;
         int64_t c = lane;
@@ -218,6 +235,7 @@ struct QuantParams {
     uint8_t *scales;
     const float *tensor_scale;
     GroupArgs g;
+    Gather gt;
     uint32_t *err;
 };
 
@@ -267,7 +285,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
         return;
     }
     const int64_t row = (int64_t)r0 + local;
-    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + row * p.stride);
+    const int64_t srow = source_row(p.gt, row, p.err);  // gathered input row
+    if (srow < 0) return;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + srow * p.stride);
     float inv = 0.0f;
     if (FMT == 0) {
         // r depends only on the block's E4M3 scale code: tabulate
@@ -484,7 +504,8 @@ __global__ void padded_offsets_kernel(const uint32_t *ro, uint32_t *so, int G) {
 // ----------------------------------------------------------------- host
 
 cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const GroupArgs &g,
-                              float *tensor_scale_out, uint32_t *err, cudaStream_t s) {
+                              const Gather &gt, float *tensor_scale_out, uint32_t *err,
+                              cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(tensor_scale_out, 0, sizeof(float) * g.num_experts, s);
     if (e != cudaSuccess) return e;
     if (g.total_rows > 0) {
@@ -493,7 +514,7 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
         int64_t warps = (g.total_rows + rows_per_warp - 1) / rows_per_warp;
         int64_t blocks = (warps + 7) / 8;
         amax_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-            reinterpret_cast<const uint16_t *>(in), stride, K, g,
+            reinterpret_cast<const uint16_t *>(in), stride, K, g, gt,
             reinterpret_cast<uint32_t *>(tensor_scale_out), err, rows_per_warp);
     }
     amax_finalize_kernel<<<(g.num_experts + 255) / 256, 256, 0, s>>>(
@@ -503,9 +524,9 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
 
 cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,
                             uint8_t *scales, const float *tensor_scale, const GroupArgs &g,
-                            uint32_t *err, cudaStream_t s) {
+                            const Gather &gt, uint32_t *err, cudaStream_t s) {
     QuantParams p{reinterpret_cast<const uint16_t *>(in), stride, K, out, scales, tensor_scale,
-                  g, err};
+                  g, gt, err};
     int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks == 0) return cudaSuccess;
     // 256-bit loads need every row start 32-byte aligned

@@ -19,13 +19,17 @@ _lib = None
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
 STATUS = {0: "MOEQ_OK", 1: "MOEQ_ERR_INVALID_ARG", 2: "MOEQ_ERR_UNSUPPORTED",
           3: "MOEQ_ERR_CUDA", 4: "MOEQ_ERR_DEVICE"}
-DEVERR_BAD_OFFSETS, DEVERR_BAD_EXPERT, DEVERR_SCALE_ROWS, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_BAD_OFFSETS, DEVERR_BAD_EXPERT, DEVERR_SCALE_ROWS, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4, 8, 16
 
 _P, _I64, _I32, _U32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)
 _SIGNATURES = {
     "moeq_grouped_amax_scale": [_P, _I64, _I64, _I64, _P, _P, _P, _I32, _I32, _P],
     "moeq_grouped_quantize": [_I32, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P,
                               _I32, _I32, _I32, _P],
+    "moeq_grouped_amax_scale_gather": [_P, _I64, _I64, _I64, _P, _I32, _I64, _P, _P, _P, _I32,
+                                       _I32, _P],
+    "moeq_grouped_quantize_gather": [_I32, _P, _I64, _I64, _I64, _P, _I32, _I64, _P, _P, _I64,
+                                     _P, _P, _P, _P, _I32, _I32, _I32, _P],
     "moeq_padded_scale_offsets": [_P, _P, _I32, _P],
     "moeq_grouped_matmul_rowwise_fp8": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
                                         _I32, _I32, _I32, _P],
@@ -128,6 +132,29 @@ def grouped_quantize(fmt, inp, out, scales, row_offsets, scales_offsets, expert_
     G = expert_ids.numel() if num_active_experts is None else num_active_experts
     _call("moeq_grouped_quantize", _fmt(fmt), _ptr_rows(inp, torch.bfloat16, "inp"), inp.stride(0),
           inp.shape[0], inp.shape[1], _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"),
+          scale_rows_total, _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32),
+          _ptr(expert_ids, torch.int32), _ptr(tensor_scale, torch.float32), num_experts,
+          max_tokens_per_expert, G, _stream(stream))
+
+
+def grouped_amax_scale_gather(inp, indices, indices_divisor, row_offsets, expert_ids,
+                              tensor_scale_out, num_experts, num_active_experts=None,
+                              stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_amax_scale_gather", _ptr_rows(inp, torch.bfloat16, "inp"), inp.stride(0),
+          inp.shape[0], inp.shape[1], _ptr(indices, torch.int32, "indices"), indices_divisor,
+          indices.numel(), _ptr(row_offsets, _U32), _ptr(expert_ids, torch.int32),
+          _ptr(tensor_scale_out, torch.float32), num_experts, G, _stream(stream))
+
+
+def grouped_quantize_gather(fmt, inp, indices, indices_divisor, out, scales, row_offsets,
+                            scales_offsets, expert_ids, tensor_scale, num_experts,
+                            scale_rows_total, max_tokens_per_expert=0, num_active_experts=None,
+                            stream=None):
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_quantize_gather", _fmt(fmt), _ptr_rows(inp, torch.bfloat16, "inp"),
+          inp.stride(0), inp.shape[0], inp.shape[1], _ptr(indices, torch.int32, "indices"),
+          indices_divisor, indices.numel(), _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"),
           scale_rows_total, _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32),
           _ptr(expert_ids, torch.int32), _ptr(tensor_scale, torch.float32), num_experts,
           max_tokens_per_expert, G, _stream(stream))

@@ -76,6 +76,7 @@ typedef enum { MOEQ_NVFP4 = 0, MOEQ_MXFP4 = 1, MOEQ_MXFP8 = 2 } moeq_format;
 #define MOEQ_DEVERR_BAD_EXPERT 0x2u  /* expert id outside [0, num_experts)   */
 #define MOEQ_DEVERR_SCALE_ROWS 0x4u  /* scale offsets unaligned / too small  */
 #define MOEQ_DEVERR_TIMEOUT 0x8u     /* a pipeline wait gave up (~1 s)       */
+#define MOEQ_DEVERR_BAD_INDEX 0x10u  /* gather index outside the input rows  */
 
 /* Per-expert NVFP4 tensor scale of the activations
  * ("grouped_quantize_dynamic_scaled_fp4_async_kernel": sf_tensor, the
@@ -128,6 +129,36 @@ moeq_status moeq_grouped_quantize(moeq_format fmt, const void *in,
                                   int32_t max_tokens_per_expert,
                                   int32_t num_active_experts,
                                   moeq_stream_t stream);
+
+/* Gather-fused variants ("max.nn.moe.NvMxf4f8Strategy", grouped_quantize:
+ * the indices and indices_divisor arguments).  Reading adopted: the rows
+ * being quantized are gathered from the input, quantized row t reading input
+ * row indices[t] / indices_divisor (e.g. indices = the expert-sorted
+ * positions token * top_k + slot and indices_divisor = top_k, so the MoE
+ * permutation needs no separate copy).  Everything else is exactly
+ * moeq_grouped_amax_scale / moeq_grouped_quantize on the gathered rows.
+ *   in          bf16 [in_rows, K], row stride in_row_stride elements.
+ *   indices     int32 [total_rows] (device); indices_divisor >= 1.
+ *   total_rows  number of quantized rows (row_offsets index these).
+ * An index whose input row falls outside [0, in_rows) skips that row and
+ * sets MOEQ_DEVERR_BAD_INDEX. */
+moeq_status moeq_grouped_amax_scale_gather(const void *in, int64_t in_row_stride,
+                                           int64_t in_rows, int64_t K,
+                                           const int32_t *indices, int32_t indices_divisor,
+                                           int64_t total_rows, const uint32_t *row_offsets,
+                                           const int32_t *expert_ids, float *tensor_scale_out,
+                                           int32_t num_experts, int32_t num_active_experts,
+                                           moeq_stream_t stream);
+
+moeq_status moeq_grouped_quantize_gather(moeq_format fmt, const void *in, int64_t in_row_stride,
+                                         int64_t in_rows, int64_t K, const int32_t *indices,
+                                         int32_t indices_divisor, int64_t total_rows,
+                                         uint8_t *out, uint8_t *scales, int64_t scale_rows_total,
+                                         const uint32_t *row_offsets,
+                                         const uint32_t *scales_offsets,
+                                         const int32_t *expert_ids, const float *tensor_scale,
+                                         int32_t num_experts, int32_t max_tokens_per_expert,
+                                         int32_t num_active_experts, moeq_stream_t stream);
 
 /* scales_offsets[g] = sum_{h<g} ceil((row_offsets[h+1]-row_offsets[h]) / 128) * 128,
  * g = 0..G (uint32 [G+1], device).  The tightest padding accepted by the

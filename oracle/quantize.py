@@ -184,6 +184,15 @@ def grouped_quantize(fmt, x, row_offsets, scales_offsets, expert_ids,
     return out, scales
 
 
+def gather_rows(x, indices, divisor):
+    """The rows the gather-fused quantizer works on ("max.nn.moe.NvMxf4f8Strategy",
+    grouped_quantize: indices, indices_divisor).  Reading adopted: row t of
+    the quantized matrix is input row indices[t] // divisor."""
+    idx = np.asarray(indices, dtype=np.int64)
+    assert divisor >= 1 and np.all(idx >= 0)
+    return np.asarray(x)[idx // int(divisor)]
+
+
 def padded_scale_offsets(row_offsets):
     """scales_offsets[g] = sum over h < g of ceil(r_h / 128) * 128."""
     ro = np.asarray(row_offsets, dtype=np.int64)

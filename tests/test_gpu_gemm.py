@@ -199,7 +199,7 @@ def run_blockscaled(fmt, a, asf, b, bsf, es, ro, so, ids, N, K, rows):
 
 @pytest.mark.parametrize("fmt,es_on", [("nvfp4", True), ("mxfp8", False), ("mxfp8", True),
                                        ("mxfp4", False), ("mxfp4", True)])
-@pytest.mark.parametrize("N,K", [(256, 512), (128, 1024)])
+@pytest.mark.parametrize("N,K", [(256, 512), (128, 1024), (512, 1536)])
 def test_blockscaled_ragged_multitile(fmt, es_on, N, K):
     need_gpu()
     from oracle import quantize as Q

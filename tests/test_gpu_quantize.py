@@ -247,3 +247,57 @@ def test_quantize_bad_device_data_sets_error_and_skips_group():
     assert moeq.get_device_error() & (moeq.DEVERR_BAD_OFFSETS | moeq.DEVERR_SCALE_ROWS)
     moeq.clear_device_error()
     assert moeq.get_device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_gather_bit_exact(fmt):
+    """Gather-fused quantize: quantized row t reads input row indices[t] / top_k
+    (expert-sorted routing positions), bit-exact against the oracle on the
+    gathered rows; also the gathered per-expert amax."""
+    need_gpu()
+    tokens, top_k, E, K = 300, 3, 8, 512
+    rng = np.random.default_rng(31)
+    experts = np.stack([rng.choice(E, top_k, replace=False) for _ in range(tokens)])
+    pos = np.arange(tokens * top_k)
+    order = np.argsort(experts.reshape(-1), kind="stable")
+    indices = pos[order].astype(np.int32)
+    counts = np.bincount(experts.reshape(-1), minlength=E)
+    ro, ids = synth.ragged_groups(counts)
+    so = Q.padded_scale_offsets(ro)
+    rows = int(so[-1])
+    x = synth.bf16_normal((tokens, K), 1.0, seed=9, outlier_p=0.01, outlier_scale=30.0)
+    xg = Q.gather_rows(x.float().numpy(), indices, top_k)
+    ts = _oracle_ts(xg, ro, ids, E)
+    T = len(indices)
+    idx_d = torch.from_numpy(indices).to(DEV)
+    amax = torch.empty(E, device=DEV)
+    moeq.grouped_amax_scale_gather(x.to(DEV), idx_d, top_k, to_dev_u32(ro), to_dev_i32(ids), amax, E)
+    assert np.array_equal(amax.cpu().numpy().view(np.uint32), ts.view(np.uint32))
+    ob = K if fmt == "mxfp8" else K // 2
+    out = torch.full((T, ob), 0xA5, dtype=torch.uint8, device=DEV)
+    sf = torch.full((moeq.sf_bytes(rows, K // _v(fmt)),), 0x5A, dtype=torch.uint8, device=DEV)
+    moeq.grouped_quantize_gather(fmt, x.to(DEV), idx_d, top_k, out, sf, to_dev_u32(ro),
+                                 to_dev_u32(so), to_dev_i32(ids), amax, E, rows)
+    want_out, want_sf = Q.grouped_quantize(fmt, xg, ro, so, ids, ts,
+                                           out=np.full((T, ob), 0xA5, np.uint8),
+                                           scales=np.full(L.physical_bytes(rows, K // _v(fmt)), 0x5A,
+                                                          np.uint8), scale_rows_total=rows)
+    assert np.array_equal(u8(out), want_out) and np.array_equal(u8(sf), want_sf)
+
+
+def test_quantize_gather_bad_index_flagged():
+    need_gpu()
+    moeq.clear_device_error()
+    K, E = 128, 2
+    ro, ids = groups_from_counts([3, 2])
+    so = Q.padded_scale_offsets(ro)
+    x = synth.bf16_normal((4, K), 1.0, seed=10)
+    indices = torch.tensor([0, 1, 9, 2, 3], dtype=torch.int32, device=DEV)   # 9 -> row 9 > 3
+    out = torch.full((5, K // 2), 0xA5, dtype=torch.uint8, device=DEV)
+    sf = torch.zeros(moeq.sf_bytes(int(so[-1]), K // 16), dtype=torch.uint8, device=DEV)
+    moeq.grouped_quantize_gather("nvfp4", x.to(DEV), indices, 1, out, sf, to_dev_u32(ro),
+                                 to_dev_u32(so), to_dev_i32(ids), torch.ones(E, device=DEV), E,
+                                 int(so[-1]))
+    assert moeq.get_device_error() & moeq.DEVERR_BAD_INDEX
+    assert (out[2] == 0xA5).all() and not (out[0] == 0xA5).all()
+    moeq.clear_device_error()

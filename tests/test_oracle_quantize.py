@@ -182,6 +182,15 @@ def test_grouped_quantize_group_permutation():
         assert np.array_equal(lgp[int(so_p[j]):int(so_p[j]) + n], lg[int(so[i]):int(so[i]) + n])
 
 
+def test_gather_rows_hand_case():
+    # routing positions token * top_k + slot with top_k = 2: positions 5, 2,
+    # 7, 0 belong to tokens 2, 1, 3, 0
+    x = np.arange(4 * 3, dtype=np.float32).reshape(4, 3)
+    got = Q.gather_rows(x, [5, 2, 7, 0], 2)
+    assert np.array_equal(got, x[[2, 1, 3, 0]])
+    assert np.array_equal(Q.gather_rows(x, [3, 1], 1), x[[3, 1]])
+
+
 def test_group_amax():
     x = np.zeros((6, 16), np.float32)
     x[0, 3] = -7
