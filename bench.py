@@ -42,6 +42,9 @@ WORKLOAD = ("NVFP4 MoE up-projection: 128 experts, 16384 tokens top-8 uniform ->
 E4, TOK4, TOPK4, K4, I4 = 128, 16384, 8, 4096, 1536
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratios
 FP8_OVER_BF16 = 4.5 / 2.25
+# DRAM bytes (read + write) of one launch of the fused GEMM on this workload,
+# from one ncu capture of the current kernel (1.21 GB read + 109.4 MB written).
+FUSED_TRAFFIC_BYTES = 1.319e9
 
 
 def parse_args():
@@ -480,7 +483,9 @@ def run_moeq(args, rank, world):
     achieved = fl / (t_f * 1e-3) / 1e12
     roof = {"kernel": "grouped_gemm_kernel<NVFP4, fused SwiGLU>", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-            "frac": round(achieved / fp4_peak, 4), "traffic": None,
+            "frac": round(achieved / fp4_peak, 4), "traffic": FUSED_TRAFFIC_BYTES,
+            "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch "
+                            "of the current kernel (one ncu pass)",
             "peak_note": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio",
             "algorithmic_flops_per_launch": fl}
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
@@ -565,11 +570,19 @@ def run_profile_case(args):
         so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
         moeq.padded_scale_offsets(ro_d, so_d)
         if args.profile == "quantize":
+            # the grouped-quantize workload itself: 8 experts, 4096 tokens
+            # top-2 -> 8192 rows, hidden 4096 (ncu flushes caches per pass)
+            counts = synth.routing_counts(4096, 2, 8, seed=0)
+            ro, ids = synth.ragged_groups(counts)
+            T, rows = int(ro[-1]), int(sum((int(c) + 127) // 128 * 128 for c in counts if c))
+            ro_d, ids_d = u32(ro), torch.from_numpy(ids).to(dev)
+            so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
+            moeq.padded_scale_offsets(ro_d, so_d)
             x = synth.bf16_normal((T, K4), 1.0, seed=1, device=dev)
-            ts = synth.uniform((32,), 0.001, 0.002, seed=2, device=dev)
+            ts = synth.uniform((8,), 0.001, 0.002, seed=2, device=dev)
             q = torch.empty((T, K4 // 2), dtype=torch.uint8, device=dev)
             sf = torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8, device=dev)
-            fn = lambda: moeq.grouped_quantize("nvfp4", x, q, sf, ro_d, so_d, ids_d, ts, 32, rows)
+            fn = lambda: moeq.grouped_quantize("nvfp4", x, q, sf, ro_d, so_d, ids_d, ts, 8, rows)
         else:
             a = synth.random_fp4_packed((T, K4 // 2), seed=1, device=dev)
             asf = synth.random_bytes(moeq.sf_bytes(rows, K4 // 16), 0x20, 0x30, seed=2, device=dev)
