@@ -491,35 +491,82 @@ def run_moeq(args, rank, world):
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
                  "fused_gemm_swiglu_ms": round(t_f, 4)}
 
-    # end to end from pinned host buffers through the same calls
+    # end to end from pinned host buffers through the same calls; steps are
+    # pipelined: the host->device copy of step i+1 (split over several copy
+    # streams) overlaps the compute of step i, device->host copies run on
+    # their own stream, two device buffer sets alternate
     xh = d["x"].cpu().pin_memory()
     roh = d["ro"].cpu().pin_memory()
     idh = d["ids"].cpu().pin_memory()
-    ch = torch.empty(d["c"].shape, dtype=torch.uint8).pin_memory()
-    sfh = torch.empty(d["csf"].shape, dtype=torch.uint8).pin_memory()
+    d_alt = dict(d)
+    for k in ("x", "ro", "ids", "so", "ts", "a", "asf", "c", "csf"):
+        d_alt[k] = torch.empty_like(d[k])
+    bufs = [d, d_alt]
+    chs = [torch.empty(d["c"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    sfhs = [torch.empty(d["csf"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    n_copy = 4
+    h2d_streams = [torch.cuda.Stream() for _ in range(n_copy)]
+    d2h_stream = torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    comp_done, d2h_done = [None, None], [None, None]
     e2e_steps = max(3, min(args.steps, 20))
 
-    def e2e_step():
-        d["x"].copy_(xh, non_blocking=True)
-        d["ro"].copy_(roh, non_blocking=True)
-        d["ids"].copy_(idh, non_blocking=True)
-        up_projection_step(d)
-        ch.copy_(d["c"], non_blocking=True)
-        sfh.copy_(d["csf"], non_blocking=True)
+    def e2e_issue(i):
+        b = i % 2
+        B = bufs[b]
+        rows = B["x"].shape[0]
+        chunk = (rows + n_copy - 1) // n_copy
+        ready = []
+        for j, st in enumerate(h2d_streams):
+            if comp_done[b] is not None:       # step i-2 has finished reading buffer b
+                st.wait_event(comp_done[b])
+            with torch.cuda.stream(st):
+                r0, r1 = j * chunk, min(rows, (j + 1) * chunk)
+                B["x"][r0:r1].copy_(xh[r0:r1], non_blocking=True)
+                if j == 0:
+                    B["ro"].copy_(roh, non_blocking=True)
+                    B["ids"].copy_(idh, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                ready.append(ev)
+        for ev in ready:
+            comp.wait_event(ev)
+        if d2h_done[b] is not None:             # outputs of step i-2 are on the host
+            comp.wait_event(d2h_done[b])
+        up_projection_step(B)
+        cd = torch.cuda.Event()
+        cd.record(comp)
+        comp_done[b] = cd
+        d2h_stream.wait_event(cd)
+        with torch.cuda.stream(d2h_stream):
+            chs[b].copy_(B["c"], non_blocking=True)
+            sfhs[b].copy_(B["csf"], non_blocking=True)
+            dd = torch.cuda.Event()
+            dd.record(d2h_stream)
+            d2h_done[b] = dd
 
-    e2e_step()
+    for i in range(2):
+        e2e_issue(i)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        e2e_issue(i)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    # plain host->device bandwidth of the activations, for context
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record()
+    d["x"].copy_(xh, non_blocking=True)
+    h1.record()
+    torch.cuda.synchronize()
     h2d = xh.numel() * 2 + roh.numel() * 4 + idh.numel() * 4
-    d2h = ch.numel() + sfh.numel()
+    d2h = chs[0].numel() + sfhs[0].numel()
     e2e = {"value": round(world * fl / e2e_s / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_s * 1e3, 3)}
+           "ms_per_step": round(e2e_s * 1e3, 3),
+           "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
+           "single_copy_h2d_GB/s": round(xh.numel() * 2 / h0.elapsed_time(h1) / 1e6, 1)}
 
     extra = {}
     if rank == 0 and not args.no_parts:
