@@ -37,8 +37,14 @@
 //    and multicasting it to both.
 //  * every wait is bounded (about one second) and sets the device error
 //    word instead of hanging.
+#include <cstring>
+
 #include "common.cuh"
 #include "launch.h"
+
+#ifndef MOEQ_SF_LOADER
+#define MOEQ_SF_LOADER 1
+#endif
 
 namespace moeq {
 
@@ -48,11 +54,12 @@ enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2, kMxfp4 = 3 };
 enum Epi { kBf16 = 0, kSwiglu = 1 };
 
 template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
-          int CM_>
+          int PAIR_, int SF_LOADER_ = 1>
 struct Cfg {
-    static constexpr int BM = 128;
-    static constexpr int CM = CM_;  // CTAs per cluster sharing (multicasting) each B tile
-    static constexpr int BN = BN_;
+    static constexpr int BM = 128;                              // rows of A per CTA
+    static constexpr int PAIR = PAIR_;                          // CTAs per MMA (cta_group)
+    static constexpr int MMA_M = BM * PAIR;
+    static constexpr int BN = BN_;                              // columns of D per tile
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;                  // TMEM accumulators
     static constexpr int BK_BYTES = 128;                        // one 128B swizzle row
@@ -64,18 +71,27 @@ struct Cfg {
     static constexpr int RB = BN >= 128 ? BN / 128 : 1;         // 128-row scale blocks of B
     static constexpr int SF_ATOMS = SCALED ? BK / SF_VEC / 4 : 0;   // atoms per 128 rows per stage
     static constexpr int SF_ATOM_BYTES = 512;
+    static constexpr int B_ROWS_CTA = BN / PAIR;                // rows of B each CTA stages
     static constexpr int A_BYTES = BM * BK_BYTES;
-    static constexpr int B_BYTES = BN * BK_BYTES;
+    static constexpr int B_BYTES = B_ROWS_CTA * BK_BYTES;
     static constexpr int SFA_BYTES = SF_ATOMS * SF_ATOM_BYTES;
+    // every CTA of a pair holds the scales of all BN rows of B: each CTA's
+    // tensor cores produce all BN columns of its rows
     static constexpr int SFB_BYTES = SF_ATOMS * SF_ATOM_BYTES * RB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int EPI_WARPS = EPI_WARPS_;
     static constexpr int EPI_GROUPS = EPI_WARPS / 4;            // epilogue warps per TMEM quarter
     static constexpr int COLS_W = BN / EPI_GROUPS;              // accumulator columns per warp
     static constexpr int CHUNKS_W = COLS_W / 32;
-    static constexpr int SF_WARPS = SCALED ? SF_WARPS_ : 0;      // warps issuing scale copies
+    // warps issuing scale copies; 0: the MMA thread copies each stage's
+    // scales right before its MMAs
+    static constexpr int SF_WARPS = SCALED ? SF_WARPS_ : 0;
     static constexpr int SF_ITEMS = SF_ATOMS * (1 + RB);         // scale atoms per stage
-    static constexpr int EPI_WARP0 = 2 + SF_WARPS;
+    // 1: a warp of its own issues the scale loads, in parallel with the A/B
+    // loads of warp 0
+    static constexpr int SF_LOADER = SCALED ? SF_LOADER_ : 0;
+    static constexpr int SF_WARP0 = 2 + SF_LOADER;
+    static constexpr int EPI_WARP0 = SF_WARP0 + SF_WARPS;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr int ACC_COLS = BN;
     static constexpr int SF_COLS_A = SF_ATOMS * 4;
@@ -91,8 +107,7 @@ struct Cfg {
     static_assert(EPI_WARPS % 4 == 0 && COLS_W % 32 == 0 && COLS_W >= 32, "epilogue split");
     static_assert(ACC_BUFS == 2 || CHUNKS_W <= 4, "single accumulator drains TMEM to registers");
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
-    static_assert(CM == 1 || (CM == 2 && BN % 256 == 0), "multicast splits B into 128-row halves");
-    static constexpr int B_ROWS_CTA = BN / CM;                  // rows of B each CTA loads
+    static_assert(PAIR == 1 || (PAIR == 2 && BN == 256), "a pair splits a 256-row B tile in halves");
 };
 
 struct Params {
@@ -152,8 +167,8 @@ __device__ __forceinline__ uint32_t group_tiles(const Params &p, int g, int NB, 
             return 0;
         }
     }
-    // a cluster of CM CTAs takes CM consecutive m-blocks of the group
-    return ((rows + C::BM - 1) / C::BM + C::CM - 1) / C::CM * (uint32_t)NB;
+    // a CTA pair takes two consecutive m-blocks of the group
+    return ((rows + C::BM - 1) / C::BM + C::PAIR - 1) / C::PAIR * (uint32_t)NB;
 }
 
 // Waits for a phase with a bound but without consulting the abort flag;
@@ -249,10 +264,38 @@ __device__ __forceinline__ void store_sf_bytes(const Params &p, int64_t prow, in
         *w = (uint8_t)bytes;
 }
 
+// Copies the scale atoms of one stage shared -> TMEM (the atoms with index
+// j % nw == w).  A atom ks -> columns 4 ks of the stage's slot; B atom
+// (rb, ks) -> columns 4 (ks RB + rb), so each MMA step reads 4 RB
+// consecutive columns covering its BN rows.  In a CTA pair the copy writes
+// each CTA's tensor memory from its own shared memory.
+template <class C>
+__device__ __forceinline__ void copy_stage_scales(uint32_t tmem, const uint8_t *smem, int stage,
+                                                  int w, int nw) {
+    const uint32_t ssfa = smem_u32(smem + stage * C::STAGE_BYTES) + C::A_BYTES + C::B_BYTES;
+    const uint32_t ssfb = ssfa + C::SFA_BYTES;
+    const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
+    const uint32_t tsfb = tsfa + C::SF_COLS_A;
+#pragma unroll
+    for (int j = 0; j < C::SF_ITEMS; ++j) {
+        if (j % nw != w) continue;
+        if (j < C::SF_ATOMS) {
+            tmem_cp_sf_atom<C::PAIR>(tsfa + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
+        } else {
+            const int i = (j - C::SF_ATOMS) / C::RB, rb = (j - C::SF_ATOMS) % C::RB;
+            tmem_cp_sf_atom<C::PAIR>(tsfb + 4 * (i * C::RB + rb),
+                                     sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
+        }
+    }
+}
+
 template <class C, int KIND, int EPI>
 __global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA,
+                        const __grid_constant__ CUtensorMap tmSFB, const Params p) {
+    constexpr bool PAIRED = C::PAIR > 1;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ uint64_t empty_bar[C::STAGES];
@@ -276,13 +319,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], C::CM);  // one MMA commit per CTA of the cluster
+            mbar_init(&full_bar[s], 1 + C::SF_LOADER);  // one arrival per loading warp
+            mbar_init(&empty_bar[s], 1);
         }
 #pragma unroll
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], C::EPI_WARPS);
+            // the even CTA's MMA thread waits for the epilogues of both CTAs
+            mbar_init(&tempty_bar[b], C::PAIR * C::EPI_WARPS);
         }
         mbar_init(&drain_bar, 1);
         mbar_init(&sf_drain_bar, C::SF_WARPS > 0 ? C::SF_WARPS : 1);  // one commit per scale warp
@@ -295,10 +339,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (PAIRED && C::SCALED) {
+            prefetch_tensormap(&tmSFA);
+            prefetch_tensormap(&tmSFB);
+        }
     }
-    if (warp == 1) {
-        tmem_alloc(&tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
+    if (warp == 1) {  // in a pair, warp 1 of both CTAs allocates collectively
+        tmem_alloc<C::PAIR>(&tmem_slot, C::TMEM_COLS);
+        tmem_relinquish<C::PAIR>();
     }
     for (int g = threadIdx.x; g < G; g += blockDim.x)
         prefix[g + 1] = group_tiles<C, EPI>(p, g, NB, blockIdx.x == 0);
@@ -320,18 +368,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Multicast clusters: the peer's barriers must be initialised before any
-    // copy or commit targets them.
-    if (C::CM > 1) cluster_sync();
+    // a pair: the other CTA's barriers must be initialised before any copy,
+    // commit or arrival targets them
+    if (PAIRED) cluster_sync();
     const uint32_t total = prefix[G];
     const uint32_t tmem = tmem_slot;
     const int KT = p.K / C::BK;
-    const uint32_t rank = C::CM > 1 ? cluster_ctarank() : 0u;   // m-block within the pair
-    const uint32_t cid = blockIdx.x / C::CM, ncl = gridDim.x / C::CM;
-    constexpr uint16_t kAll = (uint16_t)((1u << C::CM) - 1u);
+    const uint32_t rank = PAIRED ? cluster_ctarank() : 0u;   // m-block within the pair
+    const uint32_t cid = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+    if (warp == 0 || (C::SF_LOADER && warp == 2)) {
+        // ------------------------------------------------ TMA producers
+        // Warp 0 loads the A and B tiles, warp 2 (or warp 0 as well, without
+        // a scale loader) the scale atoms; both arrive on the stage's full
+        // barrier with their byte counts.  Both CTAs of a pair load their own
+        // A rows, their half of the B rows and all of the tile's scales; the
+        // copies complete on the even CTA's full barrier, which expects the
+        // bytes of both.
+        const bool do_ab = warp == 0;
+        const bool do_sf = C::SCALED && (warp == 2 || !C::SF_LOADER);
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b = policy_evict_last();
@@ -344,55 +399,67 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             bool ok = true;
             for (uint32_t t = cid; ok && t < total; t += ncl) {
                 const Tile tl = decode_tile(prefix, G, t, NB);
-                const int mb = tl.mb * C::CM + (int)rank;
+                const int mb = tl.mb * C::PAIR + (int)rank;
                 const int e = __ldg(p.expert_ids + tl.g);
                 const int row0 = (int)__ldg(p.a_offsets + tl.g) + mb * C::BM;
                 const int n0 = tl.nb * C::BN;
                 int64_t sfa0 = 0, sfb0 = 0;
                 int rbs = 1;  // scale row-blocks of B present in this tile
                 if (C::SCALED) {
-                    // an m-block past the group's end (the second CTA of a
-                    // cluster on a group with an odd m-block count) computes
+                    // an m-block past the group's end (the odd CTA of a pair
+                    // on a group with an odd m-block count) computes
                     // discarded rows: point its A scales at a real m-block so
-                    // the bulk copy stays inside the scale buffer
+                    // the copy stays inside the scale buffer
                     const uint32_t rgp = __ldg(p.a_offsets + tl.g + 1) - __ldg(p.a_offsets + tl.g);
                     const int mlast = (int)((rgp + C::BM - 1) / C::BM) - 1;
                     sfa0 = ((int64_t)(__ldg(p.a_sf_offsets + tl.g) >> 7) + min(mb, mlast)) * kv_atoms;
                     sfb0 = ((int64_t)e * nrb + n0 / 128) * kv_atoms;
                     rbs = min(C::RB, nrb - n0 / 128);
                 }
-                const uint32_t tx = C::A_BYTES + C::B_BYTES + C::SFA_BYTES +
-                                    (uint32_t)rbs * C::SF_ATOMS * C::SF_ATOM_BYTES;
+                const uint32_t tx =
+                    (do_ab ? (uint32_t)(C::A_BYTES + C::B_BYTES) : 0u) +
+                    (do_sf ? (uint32_t)(C::SFA_BYTES + rbs * C::SF_ATOMS * C::SF_ATOM_BYTES) : 0u);
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_v, p.err)) {
+                    if (!mbar_wait<PAIRED>(&empty_bar[stage], phase ^ 1u, abort_v, p.err)) {
                         ok = false;
                         break;
                     }
                     uint8_t *sa = smem + stage * C::STAGE_BYTES;
                     uint8_t *sb = sa + C::A_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[stage], C::SCALED ? tx : (uint32_t)(C::A_BYTES + C::B_BYTES));
-                    tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
-                    if (C::CM == 1) {
-                        tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
-                    } else {  // this CTA's half of B, delivered to both CTAs
-                        tma_load_3d_mc(sb + rank * C::B_ROWS_CTA * C::BK_BYTES, &tmB,
-                                       &full_bar[stage], kt * C::BK_BYTES,
-                                       n0 + (int)rank * C::B_ROWS_CTA, e, kAll, pol_b);
-                    }
-                    if (C::SCALED) {
-                        uint8_t *ssfa = sb + C::B_BYTES;
-                        uint8_t *ssfb = ssfa + C::SFA_BYTES;
-                        bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
-                                  C::SFA_BYTES, &full_bar[stage]);
-                        if (C::CM == 1) {
+                    uint8_t *ssfa = sb + C::B_BYTES;
+                    uint8_t *ssfb = ssfa + C::SFA_BYTES;
+                    if (!PAIRED) {
+                        mbar_arrive_expect_tx(&full_bar[stage], tx);
+                        if (do_ab) {
+                            tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
+                            tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
+                        }
+                        if (do_sf) {
+                            bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
+                                      C::SFA_BYTES, &full_bar[stage]);
                             for (int rb = 0; rb < rbs; ++rb)
                                 bulk_load(ssfb + rb * C::SF_ATOMS * 512,
                                           p.b_sf + (sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
                                           C::SF_ATOMS * 512, &full_bar[stage]);
-                        } else if ((int)rank < rbs) {  // scale row-block `rank`, to both CTAs
-                            bulk_load_mc(ssfb + rank * C::SF_ATOMS * 512,
-                                         p.b_sf + (sfb0 + rank * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 512,
-                                         C::SF_ATOMS * 512, &full_bar[stage], kAll);
+                        }
+                    } else {
+                        const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2u * tx);
+                        if (do_ab) {
+                            tma_load_2d_pair(sa, &tmA, fb, kt * C::BK_BYTES, row0, pol_a);
+                            tma_load_3d_pair(sb, &tmB, fb, kt * C::BK_BYTES,
+                                             n0 + (int)rank * C::B_ROWS_CTA, e, pol_b);
+                        }
+                        if (do_sf) {
+                            // scale buffers viewed as rows of 256 bytes: an
+                            // atom is two rows
+                            tma_load_2d_pair(ssfa, &tmSFA, fb, 0,
+                                             (int)((sfa0 + (int64_t)kt * C::SF_ATOMS) * 2), pol_a);
+                            for (int rb = 0; rb < rbs; ++rb)
+                                tma_load_2d_pair(
+                                    ssfb + rb * C::SF_ATOMS * 512, &tmSFB, fb, 0,
+                                    (int)((sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 2),
+                                    pol_b);
                         }
                     }
                     issued |= 1u << stage;
@@ -403,14 +470,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            if (!ok) {  // let every issued copy land before the CTA can exit
+            // let every copy this CTA's barrier counts land before the CTA
+            // can exit (the odd CTA of a pair has none: its copies complete
+            // on the even CTA's barrier, which that CTA drains)
+            if (!ok && rank == 0) {
                 for (int s = 0; s < C::STAGES; ++s)
                     if (issued & (1u << s)) mbar_drain(&full_bar[s], (issued_par >> s) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (the even CTA of a pair issues the MMAs of both)
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t it = 0;
@@ -418,18 +489,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (uint32_t t = cid; ok && t < total; t += ncl, ++it) {
                 const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
                 const uint32_t aph = C::ACC_BUFS == 2 ? ((it >> 1) & 1u) : (it & 1u);
-                if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_v, p.err)) break;
+                if (!mbar_wait<PAIRED>(&tempty_bar[buf], aph ^ 1u, abort_v, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * C::ACC_COLS;
                 for (int kt = 0; kt < KT; ++kt) {
-                    // block-scaled: the scale warp signals once the stage's
-                    // operands have landed and its scales are in TMEM
-                    if (!mbar_wait(C::SCALED ? &sf_bar[stage] : &full_bar[stage], phase, abort_v,
-                                   p.err)) {
+                    // with scale warps, they signal once the stage's operands
+                    // have landed and its scales are in TMEM
+                    const bool waited = C::SF_WARPS
+                                            ? mbar_wait(&sf_bar[stage], phase, abort_v, p.err)
+                                            : mbar_wait<PAIRED>(&full_bar[stage], phase, abort_v,
+                                                                p.err);
+                    if (!waited) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    if (C::SCALED && C::SF_WARPS == 0) copy_stage_scales<C>(tmem, smem, stage, 0, 1);
                     const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t sb = sa + C::A_BYTES;
                     const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
@@ -440,74 +515,62 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const uint64_t bd = sdesc_sw128(sb + ks * 32);
                         const uint32_t acc = (kt | ks) ? 1u : 0u;
                         if (KIND == kFp8Rowwise) {
-                            mma_f8f6f4(d, ad, bd, idesc_f8_e4m3(C::BM, C::BN), acc);
+                            mma_f8f6f4<C::PAIR>(d, ad, bd, idesc_f8_e4m3(C::MMA_M, C::BN), acc);
                         } else if (KIND == kNvfp4) {
-                            mma_nvf4(d, ad, bd, idesc_nvf4(C::BM, C::BN), tsfa + 4 * ks,
-                                     tsfb + 4 * C::RB * ks, acc);
+                            mma_nvf4<C::PAIR>(d, ad, bd, idesc_nvf4(C::MMA_M, C::BN), tsfa + 4 * ks,
+                                              tsfb + 4 * C::RB * ks, acc);
                         } else if (KIND == kMxfp4) {
                             // scale atom ks / 2 holds 4 blocks of 32 = two K=64 steps
-                            mma_mxf4(d, ad, bd, idesc_mxf4(C::BM, C::BN, (ks & 1) * 2),
-                                     tsfa + 4 * (ks >> 1), tsfb + 4 * C::RB * (ks >> 1), acc);
+                            mma_mxf4<C::PAIR>(d, ad, bd, idesc_mxf4(C::MMA_M, C::BN, (ks & 1) * 2),
+                                              tsfa + 4 * (ks >> 1), tsfb + 4 * C::RB * (ks >> 1),
+                                              acc);
                         } else {
-                            mma_mxf8(d, ad, bd, idesc_mxf8_e4m3(C::BM, C::BN, ks), tsfa, tsfb,
-                                     acc);
+                            mma_mxf8<C::PAIR>(d, ad, bd, idesc_mxf8_e4m3(C::MMA_M, C::BN, ks), tsfa,
+                                              tsfb, acc);
                         }
                     }
-                    if (C::CM == 1)
+                    // the stage is free in both CTAs once these MMAs are done
+                    if (!PAIRED)
                         tc_commit(&empty_bar[stage]);
-                    else  // the stage is free once every CTA of the cluster consumed it
-                        tc_commit_mc(&empty_bar[stage], kAll);
+                    else
+                        tc_commit_mc<2>(&empty_bar[stage], 0x3);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit(&tfull_bar[buf]);
+                if (ok) {
+                    if (!PAIRED)
+                        tc_commit(&tfull_bar[buf]);
+                    else
+                        tc_commit_mc<2>(&tfull_bar[buf], 0x3);
+                }
             }
             // every tcgen05 operation issued here completes before TMEM is freed
-            tc_commit(&drain_bar);
+            tc_commit<C::PAIR>(&drain_bar);
             mbar_drain(&drain_bar, 0);
         }
-    } else if (C::SF_WARPS && warp >= 2 && warp < C::EPI_WARP0) {
+    } else if (C::SF_WARPS && warp >= C::SF_WARP0 && warp < C::EPI_WARP0) {
         // ------------------------------------------------ scale copies
         // Copies each stage's scale atoms shared -> TMEM (tcgen05.cp) ahead of
         // the MMA thread and publishes them with tcgen05.commit on sf_bar.
         // A stage's TMEM scale slot is rewritten only after full_bar of its
         // next use, which the producer can only reach after the MMAs that
         // read the slot have completed (empty_bar), so the slot is free.
-        const int sfw = warp - 2;
-        if (lane == 0) {
+        const int sfw = warp - C::SF_WARP0;
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             for (uint32_t t = cid; t < total; t += ncl) {
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&full_bar[stage], phase, abort_v, p.err)) {
+                    if (!mbar_wait<PAIRED>(&full_bar[stage], phase, abort_v, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t ssfa =
-                        smem_u32(smem + stage * C::STAGE_BYTES) + C::A_BYTES + C::B_BYTES;
-                    const uint32_t ssfb = ssfa + C::SFA_BYTES;
-                    const uint32_t tsfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
-                    const uint32_t tsfb = tsfa + C::SF_COLS_A;
-                    // A atom ks -> columns 4 ks; B atom (rb, ks) -> columns
-                    // 4 (ks RB + rb), so each MMA step reads 4 RB
-                    // consecutive columns covering its N rows.  The atoms
-                    // of a stage are dealt round-robin over the scale warps.
-#pragma unroll
-                    for (int j = 0; j < C::SF_ITEMS; ++j) {
-                        if (j % C::SF_WARPS != sfw) continue;
-                        if (j < C::SF_ATOMS) {
-                            tmem_cp_sf_atom(tsfa + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
-                        } else {
-                            const int i = (j - C::SF_ATOMS) / C::RB, rb = (j - C::SF_ATOMS) % C::RB;
-                            tmem_cp_sf_atom(tsfb + 4 * (i * C::RB + rb),
-                                            sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
-                        }
-                    }
-                    tc_commit(&sf_bar[stage]);
+                    copy_stage_scales<C>(tmem, smem, stage, sfw, C::SF_WARPS);
+                    tc_commit<C::PAIR>(&sf_bar[stage]);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -515,14 +578,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 if (!ok) break;
             }
-            tc_commit(&sf_drain_bar);
+            tc_commit<C::PAIR>(&sf_drain_bar);
             mbar_drain(&sf_drain_bar, 0);
         }
-    } else {
+    } else if (warp >= C::EPI_WARP0) {
         // ------------------------------------------------ epilogue
         const int quad = warp & 3;
         const int cgrp = (warp - C::EPI_WARP0) >> 2;  // column group of this warp
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        // accumulator release: on the even CTA's barrier
+        const uint32_t tempty0 = PAIRED ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
+        auto release = [&](uint32_t buf) {
+            if (!PAIRED)
+                mbar_arrive(&tempty_bar[buf]);
+            else
+                mbar_arrive_cluster(tempty0 + 8u * buf);
+        };
         uint32_t it = 0;
         for (uint32_t t = cid; t < total; t += ncl, ++it) {
             const uint32_t buf = C::ACC_BUFS == 2 ? (it & 1u) : 0u;
@@ -531,7 +602,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int e = __ldg(p.expert_ids + tl.g);
             const uint32_t r0 = __ldg(p.a_offsets + tl.g);
             const uint32_t rg = __ldg(p.a_offsets + tl.g + 1) - r0;
-            const int mb = tl.mb * C::CM + (int)rank;
+            const int mb = tl.mb * C::PAIR + (int)rank;
             // scale rows of this m-block exist only if the group reaches it
             const bool mb_in_group = (uint32_t)mb * C::BM < rg;
             const uint32_t lrow = (uint32_t)(mb * C::BM + quad * 32 + lane);
@@ -545,7 +616,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 rs = __ldg(p.expert_scales + e);
             }
             if (EPI == kSwiglu) inv_out = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + e));
-            if (!mbar_wait(&tfull_bar[buf], aph, abort_v, p.err)) break;
+            if (!mbar_wait<PAIRED>(&tfull_bar[buf], aph, abort_v, p.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + lane_off + buf * C::ACC_COLS + cgrp * C::COLS_W;
             uint32_t sfbytes = 0;
@@ -554,7 +625,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // not a multiple of BN): nothing to read or write
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                if (lane == 0) release(buf);
                 continue;
             }
             if (C::ACC_BUFS == 1) {
@@ -566,7 +637,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                if (lane == 0) release(buf);
 #pragma unroll
                 for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
                     sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
@@ -581,7 +652,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (ch == C::CHUNKS_W - 1) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                        if (lane == 0) release(buf);
                     }
                     const uint32_t code = epilogue_chunk<C, KIND, EPI>(
                         p, r, ncol0 + ch * 32, e, row, valid, rs, inv_out);
@@ -605,12 +676,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    // no CTA leaves while its peer may still multicast into it
-    if (C::CM > 1) cluster_sync();
+    // neither CTA of a pair leaves while the other may still target it
+    if (PAIRED) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc<C::PAIR>(tmem, C::TMEM_COLS);
     }
 }
 
@@ -648,6 +719,23 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims
     return r == CUDA_SUCCESS;
 }
 
+// uint8 tensor map over `bytes` bytes viewed as rows of 256 bytes (no
+// swizzle), boxes of box_rows rows: the scale buffers, whose 512-byte atoms
+// are two such rows.
+bool make_flat_map(CUtensorMap *m, const void *base, int64_t bytes, cuuint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int64_t rows = bytes / 256 > 0 ? bytes / 256 : 1;
+    cuuint64_t dims[2] = {256, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cache[64] = {0};
     int dev = 0;
@@ -662,19 +750,28 @@ int sm_count() {
 }
 
 template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1,
-          int CM = 1>
+          int PAIR = 1>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, CM>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, PAIR, MOEQ_SF_LOADER>;
     const int64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
-    CUtensorMap tA, tB;
+    CUtensorMap tA, tB, tSFA, tSFB;
+    memset(&tSFA, 0, sizeof(tSFA));
+    memset(&tSFB, 0, sizeof(tSFB));
     cuuint64_t da[2] = {(cuuint64_t)kbytes, (cuuint64_t)T};
     cuuint64_t sa[1] = {(cuuint64_t)kbytes};
     cuuint64_t db[3] = {(cuuint64_t)kbytes, (cuuint64_t)a.N, (cuuint64_t)E};
     cuuint64_t sb[2] = {(cuuint64_t)kbytes, (cuuint64_t)(kbytes * a.N)};
     if (!make_map(&tA, a.a, 2, da, sa, C::BM)) return cudaErrorInvalidValue;
     if (!make_map(&tB, a.b, 3, db, sb, C::B_ROWS_CTA)) return cudaErrorInvalidValue;
+    if (PAIR > 1 && C::SCALED) {
+        const int64_t kv_atoms = a.K / C::SF_VEC / 4;
+        const int64_t sfa_bytes = a.groups.scale_rows_total / 128 * kv_atoms * 512;
+        const int64_t sfb_bytes = E * ((a.N + 127) / 128) * kv_atoms * 512;
+        if (!make_flat_map(&tSFA, a.a_sf, sfa_bytes, 2 * C::SF_ATOMS)) return cudaErrorInvalidValue;
+        if (!make_flat_map(&tSFB, a.b_sf, sfb_bytes, 2 * C::SF_ATOMS)) return cudaErrorInvalidValue;
+    }
     Params p;
     p.a_offsets = a.groups.row_offsets;
     p.a_sf_offsets = a.groups.scales_offsets;
@@ -696,22 +793,22 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     p.c_sf = a.c_sf;
     p.err = a.err;
     const int64_t nb = (a.N + BN - 1) / BN;
-    // upper bound of the tiles (cluster tiles for CM > 1) the offsets can give
-    const int64_t tiles_ub = (T / (C::BM * CM) + a.groups.num_groups) * nb;
+    // upper bound of the tiles (pair tiles for PAIR > 1) the offsets can give
+    const int64_t tiles_ub = (T / (C::BM * PAIR) + a.groups.num_groups) * nb;
     auto kern = grouped_gemm_kernel<C, KIND, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (CM == 1) {
+    if (PAIR == 1) {
         const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
-        kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, p);
+        kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, tSFA, tSFB, p);
         return cudaGetLastError();
     }
-    // persistent clusters of CM CTAs: as many as can be resident at once
+    // persistent CTA pairs (clusters of two): as many as can be resident
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.x = PAIR;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -719,14 +816,14 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)(sm_count() / CM * CM), 1, 1);
+    cfg.gridDim = dim3((unsigned)(sm_count() / PAIR * PAIR), 1, 1);
     int max_clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorNotSupported;
     int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
-    cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, tA, tB, p);
+    cfg.gridDim = dim3((unsigned)(clusters * PAIR), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSFA, tSFB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -764,29 +861,38 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 #ifndef MOEQ_SF_WARPS
 #define MOEQ_SF_WARPS 1
 #endif
-#ifndef MOEQ_GEMM_CM
-#define MOEQ_GEMM_CM 1
+#ifndef MOEQ_GEMM_PAIR
+#define MOEQ_GEMM_PAIR 1
+#endif
+#ifndef MOEQ_FP4_PAIR_STAGES
+#define MOEQ_FP4_PAIR_STAGES 5
+#endif
+#ifndef MOEQ_FP8_PAIR_STAGES
+#define MOEQ_FP8_PAIR_STAGES 6
 #endif
 #ifndef MOEQ_MX8_STAGES
 #define MOEQ_MX8_STAGES 6
 #endif
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
+    constexpr int P = MOEQ_GEMM_PAIR;
+    constexpr int FP4_ST = P == 2 ? MOEQ_FP4_PAIR_STAGES : MOEQ_FP4_STAGES;
+    constexpr int FP8_ST = P == 2 ? MOEQ_FP8_PAIR_STAGES : MOEQ_FP8_STAGES;
     if (a.kind == kFp8Rowwise && a.epi == kBf16) {
         if (a.N >= 256)
-            return run_gemm<kFp8Rowwise, kBf16, MOEQ_FP8_BN, MOEQ_FP8_STAGES, 2,
-                            MOEQ_FP8_EPI_WARPS, 1, MOEQ_GEMM_CM>(a, s);
+            return run_gemm<kFp8Rowwise, kBf16, MOEQ_FP8_BN, FP8_ST, 2, MOEQ_FP8_EPI_WARPS, 1, P>(
+                a, s);
         return run_gemm<kFp8Rowwise, kBf16, 64, 8, 2, 4>(a, s);
     }
     if (a.kind == kNvfp4 && a.epi == kBf16)
-        return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS, MOEQ_GEMM_CM>(a, s);
+        return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
+                        MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
-        return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, MOEQ_GEMM_CM>(a, s);
+        return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp4 && a.epi == kBf16)
-        return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, MOEQ_FP4_STAGES, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS>(a, s);
+        return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
+                        MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp8 && a.epi == kBf16)
         return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;
