@@ -122,15 +122,6 @@ __device__ __forceinline__ uint32_t bf16_abs_max8(const uint4 &v) {
     return m;
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&x)[8]) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-}
-
 // floor(log2(v)) of a non-zero non-negative bf16 given by its bits.
 __device__ __forceinline__ int bf16_floor_log2(uint32_t b) {
     int ef = (int)((b >> 7) & 0xFFu);
@@ -171,6 +162,23 @@ __device__ __forceinline__ int64_t source_row(const Gather &gt, int64_t row, uin
     return s;
 }
 
+// max |x| over one row of K bf16 as a bf16 bit pattern (NaN sorts above
+// inf), the same value in every lane of the warp.
+__device__ __forceinline__ uint32_t row_abs_max(const uint4 *src, int64_t K, int lane) {
+    uint32_t m = 0;
+    const int64_t n16 = K / 8;
+    int64_t c = lane;
+    for (; c + 7 * 32 < n16; c += 8 * 32) {  // 8 independent loads in flight
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = ld_stream(src + c + u * 32);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = max(m, bf16_abs_max8(v[u]));
+    }
+    for (; c < n16; c += 32) m = max(m, bf16_abs_max8(ld_stream(src + c)));
+    return __reduce_max_sync(0xFFFFFFFFu, m);
+}
+
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ in,
                                                    int64_t stride, int64_t K, GroupArgs g,
                                                    Gather gt,
@@ -194,19 +202,8 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ 
         const int e = gv.eid[gi];
         const int64_t srow = source_row(gt, row, err);
         if (srow < 0) continue;
-        const uint4 *src = reinterpret_cast<const uint4 *>(in + srow * stride);
-        uint32_t m = 0;
-        const int64_t n16 = K / 8;
-        int64_t c = lane;
-        for (; c + 7 * 32 < n16; c += 8 * 32) {  // 8 independent loads in flight
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = ld_stream(src + c + u * 32);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) m = max(m, bf16_abs_max8(v[u]));
-        }
-        for (; c < n16; c += 32) m = max(m, bf16_abs_max8(ld_stream(src + c)));
-        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        const uint32_t m =
+            row_abs_max(reinterpret_cast<const uint4 *>(in + srow * stride), K, lane);
         if (e != cur_e) {
             if (cur_e >= 0 && lane == 0 && cur_m) atomicMax(amax_bits + cur_e, cur_m << 16);
             cur_e = e;
@@ -261,6 +258,75 @@ __device__ __forceinline__ uint32_t bf16_abs_max16(const uint32_t (&w)[8]) {
     return max(m[0] & 0xFFFFu, m[0] >> 16);
 }
 
+// The 32 bytes (16 bf16) of one 512-element step that a lane reads.
+template <bool A32>
+__device__ __forceinline__ void load_step(const uint8_t *a, uint32_t (&w)[8]) {
+    if (A32) {  // row starts are 32-byte aligned: one 256-bit load
+        ld_stream32(a, w);
+    } else {
+        const uint4 lo = ld_stream(a), hi = ld_stream(a + 16);
+        w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+        w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+    }
+}
+
+// NVFP4 quantization of one row of K bf16 (one warp): lane i takes elements
+// [16 i, 16 i + 16) of each 512-element step, a whole block.  Codes go to
+// out_row, the E4M3 block scales to logical scale row prow.  r_tab[c] =
+// inv / value(c) for every E4M3 code c (0 where the block scale is 0).
+template <bool A32>
+__device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *out_row,
+                                                   uint8_t *scales, int64_t prow, int64_t K,
+                                                   float inv, const float *r_tab, int lane) {
+    const int64_t kv_atoms = K / 64;
+    const int nsteps = (int)((K + 511) / 512);
+    const int lanes_last = (int)(K / 16 - (int64_t)(nsteps - 1) * 32);
+    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
+    for (int s0 = 0; s0 < nsteps; s0 += U) {
+        uint32_t w[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            const int s = s0 + u;
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u;
+            if (s >= nsteps) break;
+            const bool active = s < nsteps - 1 || lane < lanes_last;
+            const uint32_t mb = bf16_abs_max16(w[u]);
+            const Nvfp4Scale sc0 = nvfp4_block_scale_code(bf16_bits_to_f32(mb), inv);
+            const float r = r_tab[sc0.code];
+            float x[8];
+            uint32_t codes[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[2 * i] = bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu);
+                    x[2 * i + 1] = __uint_as_float(w[u][4 * h + i] & 0xFFFF0000u);
+                }
+                codes[h] = nvfp4_codes8(x, r);
+            }
+            const uint32_t word = gather4(sc0.code, lane, 1);
+            if (!active) continue;
+            reinterpret_cast<uint2 *>(out_row)[s * 32 + lane] = make_uint2(codes[0], codes[1]);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<uint32_t *>(
+                    scales + sf_word_offset(prow, s * 8 + (lane >> 2), kv_atoms)) = word;
+        }
+    }
+}
+
+// Entry c of the NVFP4 multiplier table: inv / value(c) for the E4M3 scale
+// code c, 0 for the zero code (and the NaN code, never produced).
+__device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
+    return (c == 0 || c >= 0x7F) ? 0.0f : __fdiv_rn(inv, e4m3_pos_value(c));
+}
+
 // fmt: 0 NVFP4, 1 MXFP4, 2 MXFP8.  One warp per logical scale row; in each
 // 512-element step lane i takes elements [16 i, 16 i + 16): a whole NVFP4
 // block, or half of an MX block (lanes 2j, 2j+1 share block j).
@@ -288,18 +354,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
     const int64_t srow = source_row(p.gt, row, p.err);  // gathered input row
     if (srow < 0) return;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + srow * p.stride);
-    float inv = 0.0f;
     if (FMT == 0) {
         // r depends only on the block's E4M3 scale code: tabulate
         // r[c] = inv / value(c) once per row (same IEEE division per entry).
-        inv = __fdiv_rn(1.0f, gv.scale(gi));
+        const float inv = __fdiv_rn(1.0f, gv.scale(gi));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t c = (uint32_t)(lane * 4 + j);
-            const float sb = e4m3_pos_value(c);
-            r_table[wid][c] = (c == 0 || c >= 0x7F) ? 0.0f : __fdiv_rn(inv, sb);
-        }
+        for (int j = 0; j < 4; ++j) r_table[wid][lane * 4 + j] = nvfp4_r_entry(lane * 4 + j, inv);
         __syncwarp();
+        nvfp4_quantize_row<A32>(src, p.out + row * (p.K / 2), p.scales, prow, p.K, inv,
+                                r_table[wid], lane);
+        return;
     }
     const int nsteps = (int)((p.K + 511) / 512);
     const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
@@ -311,16 +375,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[u][i] = 0u;
             const int s = s0 + u;
-            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last)) {
-                const uint8_t *a = src + (int64_t)s * 1024 + lane * 32;
-                if (A32) {  // row starts are 32-byte aligned: one 256-bit load
-                    ld_stream32(a, w[u]);
-                } else {
-                    const uint4 lo = ld_stream(a), hi = ld_stream(a + 16);
-                    w[u][0] = lo.x; w[u][1] = lo.y; w[u][2] = lo.z; w[u][3] = lo.w;
-                    w[u][4] = hi.x; w[u][5] = hi.y; w[u][6] = hi.z; w[u][7] = hi.w;
-                }
-            }
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -328,29 +384,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
             if (s >= nsteps) break;
             const bool active = s < nsteps - 1 || lane < lanes_last;
             uint32_t mb = bf16_abs_max16(w[u]);
-            if (FMT == 0) {
-                const Nvfp4Scale sc0 = nvfp4_block_scale_code(bf16_bits_to_f32(mb), inv);
-                const float r = r_table[wid][sc0.code];
-                float x[8];
-                uint32_t codes[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x[2 * i] = bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu);
-                        x[2 * i + 1] = __uint_as_float(w[u][4 * h + i] & 0xFFFF0000u);
-                    }
-                    codes[h] = nvfp4_codes8(x, r);
-                }
-                const uint32_t word = gather4(sc0.code, lane, 1);
-                if (!active) continue;
-                reinterpret_cast<uint2 *>(p.out + row * (p.K / 2))[s * 32 + lane] =
-                    make_uint2(codes[0], codes[1]);
-                if ((lane & 3) == 0)
-                    *reinterpret_cast<uint32_t *>(
-                        p.scales + sf_word_offset(prow, s * 8 + (lane >> 2), kv_atoms)) = word;
-            } else {
-                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));  // block = lanes 2j, 2j+1
+            {  // MX block: lanes 2j and 2j+1
+                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
                 constexpr int emax = FMT == 2 ? 8 : 2;
                 uint32_t code = 0;
                 float f = 0.0f;
