@@ -66,6 +66,56 @@ __device__ __forceinline__ float e4m3_pos_value(uint32_t code) {
     return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
+// ------------------------------------------- paired fp32 arithmetic (f32x2)
+// Two independent IEEE fp32 operations per instruction (round to nearest
+// even, subnormals kept): each lane gives exactly the scalar result.
+struct F2 {
+    uint64_t v;
+};
+
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float f2_lo(F2 a) {
+    float lo;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(a.v));
+    return lo;
+}
+
+__device__ __forceinline__ float f2_hi(F2 a) {
+    float hi;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(a.v));
+    return hi;
+}
+
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+    F2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+    F2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
+__device__ __forceinline__ F2 sub2(F2 a, F2 b) {
+    F2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
+// Two fp32 -> bf16 (round to nearest even) -> fp32.
+__device__ __forceinline__ F2 round_bf16_2(F2 a) {
+    uint32_t b;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(f2_hi(a)), "f"(f2_lo(a)));
+    return f2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
+}
+
 // ------------------------------------------------------- NVFP4 block rule
 // One 16-element block: amax m, per-expert inverse tensor scale inv.
 // sb = E4M3((m * inv) / 6); r = inv / sb; codes = E2M1(x * r) (all +0 when
@@ -93,12 +143,19 @@ __device__ __forceinline__ Nvfp4Scale nvfp4_block_scale_code(float m, float inv)
     return s;
 }
 
-// Eight elements of a block -> 32 bits of packed codes.
+
+// Eight elements of a block -> 32 bits of packed codes (the products x * r
+// in paired multiplies: the same IEEE products as scalar code).
 __device__ __forceinline__ uint32_t nvfp4_codes8(const float (&x)[8], float r) {
     if (r == 0.0f) return 0u;
+    const F2 r2 = f2(r, r);
     float y[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[i], r);
+    for (int i = 0; i < 8; i += 2) {
+        const F2 q = mul2(f2(x[i], x[i + 1]), r2);
+        y[i] = f2_lo(q);
+        y[i + 1] = f2_hi(q);
+    }
     return e2m1x8(y);
 }
 
@@ -145,6 +202,49 @@ __device__ __forceinline__ float exp_spec(float x) {
 __device__ __forceinline__ float silu_spec(float g) {
     return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
 }
+
+// exp_spec of two arguments, the same steps in paired arithmetic: each
+// result equals exp_spec of its argument bit for bit.
+__device__ __forceinline__ F2 exp_spec2(float x0, float x1) {
+    const F2 kLog2e = f2(1.44269502162933349609375f, 1.44269502162933349609375f);
+    const F2 kLn2Hi = f2(0.693145751953125f, 0.693145751953125f);
+    const F2 kLn2Lo = f2(1.428606765330187045037746429443359375e-06f,
+                         1.428606765330187045037746429443359375e-06f);
+    const float c[8] = {1.0f, 1.0f, 0.5f, 0.16666667163372039794921875f,
+                        0.0416666679084300994873046875f, 0.008333333767950534820556640625f,
+                        0.001388888922519981861114501953125f,
+                        0.0001984127011382952332496643066406f};
+    const float xc0 = fminf(fmaxf(x0, -104.0f), 89.0f);
+    const float xc1 = fminf(fmaxf(x1, -104.0f), 89.0f);
+    const F2 xc = f2(xc0, xc1);
+    const F2 t = mul2(xc, kLog2e);
+    const float n0 = rintf(f2_lo(t)), n1 = rintf(f2_hi(t));
+    const F2 n = f2(n0, n1);
+    F2 f = sub2(xc, mul2(n, kLn2Hi));
+    f = sub2(f, mul2(n, kLn2Lo));
+    F2 p = f2(c[7], c[7]);
+#pragma unroll
+    for (int k = 6; k >= 0; --k) p = add2(mul2(p, f), f2(c[k], c[k]));
+    const int i0 = (int)n0, i1 = (int)n1;
+    const int a0 = i0 >> 1, a1 = i1 >> 1;
+    const F2 s1 = f2(__int_as_float((a0 + 127) << 23), __int_as_float((a1 + 127) << 23));
+    const F2 s2 = f2(__int_as_float((i0 - a0 + 127) << 23), __int_as_float((i1 - a1 + 127) << 23));
+    const F2 r = mul2(mul2(p, s1), s2);
+    float r0 = f2_lo(r), r1 = f2_hi(r);
+    r0 = (x0 >= 89.0f) ? __int_as_float(0x7f800000) : r0;
+    r1 = (x1 >= 89.0f) ? __int_as_float(0x7f800000) : r1;
+    return f2((x0 <= -104.0f) ? 0.0f : r0, (x1 <= -104.0f) ? 0.0f : r1);
+}
+
+// h = silu_spec(g) * u for two (gate, up) pairs, bit-identical to the
+// scalar steps.
+__device__ __forceinline__ F2 swiglu2(float g0, float g1, float u0, float u1) {
+    const F2 den = add2(f2(1.0f, 1.0f), exp_spec2(-g0, -g1));
+    const F2 sl = f2(__fdiv_rn(g0, f2_lo(den)), __fdiv_rn(g1, f2_hi(den)));
+    return mul2(sl, f2(u0, u1));
+}
+
+
 
 // ----------------------------------------------------- tiled scale layout
 // Byte offset of the 4-byte word holding scale columns [4 kb, 4 kb + 4) of

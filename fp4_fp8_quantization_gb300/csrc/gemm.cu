@@ -223,13 +223,19 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
         }
         return 0u;
     } else {
+        // h = silu(gate) * up with gate, up = bf16(acc * scale), in paired
+        // fp32 arithmetic (bit-identical to the scalar definition)
         float h[16];
+        const F2 rs2 = f2(rs, rs);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float gt = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i]), rs)));
-            float up =
-                bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__uint_as_float(r[2 * i + 1]), rs)));
-            h[i] = __fmul_rn(silu_spec(gt), up);
+        for (int i = 0; i < 16; i += 2) {
+            const F2 q0 = round_bf16_2(
+                mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2));
+            const F2 q1 = round_bf16_2(
+                mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2));
+            const F2 hh = swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
+            h[i] = f2_lo(hh);
+            h[i + 1] = f2_hi(hh);
         }
         float m = 0.0f;
 #pragma unroll

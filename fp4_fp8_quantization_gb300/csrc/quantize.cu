@@ -485,10 +485,12 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
             const uint4 v0 = v[u][0], v1 = v[u][1];
             uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float gate = bf16_bits_to_f32(w[i] & 0xFFFFu);
-                float up = bf16_bits_to_f32(w[i] >> 16);
-                h[i] = __fmul_rn(silu_spec(gate), up);
+            for (int i = 0; i < 8; i += 2) {  // (gate, up) pairs, two at a time
+                const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
+                                      bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
+                                      bf16_bits_to_f32(w[i] >> 16), bf16_bits_to_f32(w[i + 1] >> 16));
+                h[i] = f2_lo(hh);
+                h[i + 1] = f2_hi(hh);
             }
         } else {
 #pragma unroll
