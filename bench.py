@@ -42,9 +42,10 @@ WORKLOAD = ("NVFP4 MoE up-projection: 128 experts, 16384 tokens top-8 uniform ->
 E4, TOK4, TOPK4, K4, I4 = 128, 16384, 8, 4096, 1536
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratios
 FP8_OVER_BF16 = 4.5 / 2.25
-# DRAM bytes (read + write) of one launch of the fused GEMM on this workload,
-# from one ncu capture of the current kernel (1.21 GB read + 109.4 MB written).
-FUSED_TRAFFIC_BYTES = 1.319e9
+# DRAM bytes (read + write) of one launch of the fused GEMM on this workload
+# from one ncu capture of the current kernel; None until the kernel as built
+# now has been captured.
+FUSED_TRAFFIC_BYTES = None
 
 
 def parse_args():
@@ -485,7 +486,7 @@ def run_moeq(args, rank, world):
             "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / fp4_peak, 4), "traffic": FUSED_TRAFFIC_BYTES,
             "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch "
-                            "of the current kernel (one ncu pass)",
+                            "of the current kernel (one ncu pass); null when not yet captured",
             "peak_note": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio",
             "algorithmic_flops_per_launch": fl}
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
