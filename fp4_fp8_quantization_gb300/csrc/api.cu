@@ -303,6 +303,30 @@ moeq_status moeq_grouped_matmul_blockscaled(
     return cuda_status(moeq::launch_gemm(ga, stream));
 }
 
+static moeq_status swiglu_quantize_impl(int out_fmt, uint8_t *c_q, uint8_t *c_sf, const void *y,
+                                        const float *out_tensor_scale, const uint32_t *a_offsets,
+                                        const uint32_t *a_scales_offsets,
+                                        const int32_t *expert_ids, int64_t total_tokens,
+                                        int64_t scale_rows_total, int64_t I, int32_t num_experts,
+                                        int32_t num_active_experts, moeq_stream_t stream) {
+    if (!groups_ok(a_offsets, expert_ids, num_experts, num_active_experts))
+        return MOEQ_ERR_INVALID_ARG;
+    if (total_tokens < 0 || I <= 0 || I % (out_fmt == 0 ? 64 : 128) || scale_rows_total < 0 ||
+        scale_rows_total % 128)
+        return MOEQ_ERR_INVALID_ARG;
+    if (out_fmt == 0 && !out_tensor_scale) return MOEQ_ERR_INVALID_ARG;
+    if (num_active_experts == 0 || total_tokens == 0 || scale_rows_total == 0) return MOEQ_OK;
+    if (!a_scales_offsets || !y || !c_q || !c_sf || !aligned16(y) || !aligned16(c_q) ||
+        !aligned16(c_sf))
+        return MOEQ_ERR_INVALID_ARG;
+    uint32_t *err = device_error_ptr();
+    if (!err) return cuda_status(cudaErrorInvalidDevice);
+    moeq::GroupArgs g = make_groups(a_offsets, a_scales_offsets, expert_ids, num_active_experts,
+                                    num_experts, total_tokens, scale_rows_total);
+    return cuda_status(moeq::launch_swiglu_quantize(out_fmt, c_q, c_sf, y, I, out_tensor_scale, g,
+                                                    err, stream));
+}
+
 moeq_status moeq_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf, const void *y,
                                  const float *out_tensor_scale, const uint32_t *a_offsets,
                                  const uint32_t *a_scales_offsets, const int32_t *expert_ids,
@@ -310,29 +334,31 @@ moeq_status moeq_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf, const void *y
                                  int32_t num_experts, int32_t max_tokens_per_expert,
                                  int32_t num_active_experts, moeq_stream_t stream) {
     (void)max_tokens_per_expert;
-    if (!groups_ok(a_offsets, expert_ids, num_experts, num_active_experts))
-        return MOEQ_ERR_INVALID_ARG;
-    if (total_tokens < 0 || I <= 0 || I % 64 || scale_rows_total < 0 || scale_rows_total % 128)
-        return MOEQ_ERR_INVALID_ARG;
-    if (!out_tensor_scale) return MOEQ_ERR_INVALID_ARG;
-    if (num_active_experts == 0 || total_tokens == 0 || scale_rows_total == 0) return MOEQ_OK;
-    if (!a_scales_offsets || !y || !c_packed || !c_sf || !aligned16(y) || !aligned16(c_packed) ||
-        !aligned16(c_sf))
-        return MOEQ_ERR_INVALID_ARG;
-    uint32_t *err = device_error_ptr();
-    if (!err) return cuda_status(cudaErrorInvalidDevice);
-    moeq::GroupArgs g = make_groups(a_offsets, a_scales_offsets, expert_ids, num_active_experts,
-                                    num_experts, total_tokens, scale_rows_total);
-    return cuda_status(
-        moeq::launch_swiglu_quantize(c_packed, c_sf, y, I, out_tensor_scale, g, err, stream));
+    return swiglu_quantize_impl(0, c_packed, c_sf, y, out_tensor_scale, a_offsets,
+                                a_scales_offsets, expert_ids, total_tokens, scale_rows_total, I,
+                                num_experts, num_active_experts, stream);
+}
+
+moeq_status moeq_swiglu_quantize_mx(moeq_format fmt, uint8_t *c_q, uint8_t *c_sf, const void *y,
+                                    const uint32_t *a_offsets, const uint32_t *a_scales_offsets,
+                                    const int32_t *expert_ids, int64_t total_tokens,
+                                    int64_t scale_rows_total, int64_t I, int32_t num_experts,
+                                    int32_t max_tokens_per_expert, int32_t num_active_experts,
+                                    moeq_stream_t stream) {
+    (void)max_tokens_per_expert;
+    if (fmt != MOEQ_MXFP4 && fmt != MOEQ_MXFP8) return MOEQ_ERR_INVALID_ARG;
+    return swiglu_quantize_impl((int)fmt, c_q, c_sf, y, nullptr, a_offsets, a_scales_offsets,
+                                expert_ids, total_tokens, scale_rows_total, I, num_experts,
+                                num_active_experts, stream);
 }
 
 moeq_status moeq_grouped_matmul_swiglu(
     uint8_t *c_packed, uint8_t *c_sf, const uint8_t *a, const uint8_t *a_sf, const uint8_t *b,
     const uint8_t *b_sf, const float *expert_scales, const float *out_tensor_scale,
-    const uint32_t *a_offsets, const uint32_t *a_scales_offsets, const int32_t *expert_ids,
-    int64_t total_tokens, int64_t scale_rows_total, int64_t I, int64_t K, int32_t num_experts,
-    int32_t max_tokens_per_expert, int32_t num_active_experts, moeq_stream_t stream) {
+    const void *a_row_scales, const uint32_t *a_offsets, const uint32_t *a_scales_offsets,
+    const int32_t *expert_ids, int64_t total_tokens, int64_t scale_rows_total, int64_t I,
+    int64_t K, int32_t num_experts, int32_t max_tokens_per_expert, int32_t num_active_experts,
+    moeq_stream_t stream) {
     if (I <= 0 || I % 64) return MOEQ_ERR_INVALID_ARG;
     moeq::GemmArgs ga;
     moeq_status st = blockscaled_common(MOEQ_NVFP4, 1, a, a_sf, b, b_sf, a_offsets,
@@ -341,6 +367,7 @@ moeq_status moeq_grouped_matmul_swiglu(
                                         num_active_experts, &ga);
     if (st != MOEQ_OK) return st;
     if (!expert_scales || !out_tensor_scale) return MOEQ_ERR_INVALID_ARG;
+    if (a_row_scales && !aligned16(a_row_scales)) return MOEQ_ERR_INVALID_ARG;
     if (num_active_experts == 0 || total_tokens == 0) return MOEQ_OK;
     if (!c_packed || !c_sf || !aligned16(c_packed) || !aligned16(c_sf))
         return MOEQ_ERR_INVALID_ARG;
@@ -348,7 +375,34 @@ moeq_status moeq_grouped_matmul_swiglu(
     if (!err) return cuda_status(cudaErrorInvalidDevice);
     ga.expert_scales = expert_scales;
     ga.out_tensor_scale = out_tensor_scale;
+    ga.row_scales = static_cast<const uint16_t *>(a_row_scales);
     ga.c_packed = c_packed;
+    ga.c_sf = c_sf;
+    ga.max_tokens_per_expert = max_tokens_per_expert;
+    ga.err = err;
+    return cuda_status(moeq::launch_gemm(ga, stream));
+}
+
+moeq_status moeq_grouped_matmul_swiglu_mx(
+    moeq_format fmt, uint8_t *c_q, uint8_t *c_sf, const uint8_t *a, const uint8_t *a_sf,
+    const uint8_t *b, const uint8_t *b_sf, const float *expert_scales, const uint32_t *a_offsets,
+    const uint32_t *a_scales_offsets, const int32_t *expert_ids, int64_t total_tokens,
+    int64_t scale_rows_total, int64_t I, int64_t K, int32_t num_experts,
+    int32_t max_tokens_per_expert, int32_t num_active_experts, moeq_stream_t stream) {
+    if (fmt != MOEQ_MXFP4 && fmt != MOEQ_MXFP8) return MOEQ_ERR_INVALID_ARG;
+    if (I <= 0 || I % 128) return MOEQ_ERR_INVALID_ARG;
+    moeq::GemmArgs ga;
+    moeq_status st = blockscaled_common(fmt, 2, a, a_sf, b, b_sf, a_offsets, a_scales_offsets,
+                                        expert_ids, total_tokens, scale_rows_total, 2 * I, K,
+                                        num_experts, num_active_experts, &ga);
+    if (st != MOEQ_OK) return st;
+    if (expert_scales && !aligned16(expert_scales)) return MOEQ_ERR_INVALID_ARG;
+    if (num_active_experts == 0 || total_tokens == 0) return MOEQ_OK;
+    if (!c_q || !c_sf || !aligned16(c_q) || !aligned16(c_sf)) return MOEQ_ERR_INVALID_ARG;
+    uint32_t *err = device_error_ptr();
+    if (!err) return cuda_status(cudaErrorInvalidDevice);
+    ga.expert_scales = expert_scales;
+    ga.c_packed = c_q;
     ga.c_sf = c_sf;
     ga.max_tokens_per_expert = max_tokens_per_expert;
     ga.err = err;

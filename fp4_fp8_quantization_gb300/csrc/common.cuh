@@ -159,6 +159,23 @@ __device__ __forceinline__ uint32_t nvfp4_codes8(const float (&x)[8], float r) {
     return e2m1x8(y);
 }
 
+// ------------------------------------------------------- MX block rule
+// Scale code of an MX block whose amax m is a positive fp32 value: the OCP
+// floor rule c = clamp(floor(log2 m) - emax + 127, 0, 254), floor(log2 m)
+// read from the fp32 exponent bits (subnormals included).  For finite m,
+// c <= 252 (emax >= 2), so the element multiplier 2^(127 - c) is a normal
+// fp32 number.
+__device__ __forceinline__ uint32_t mx_scale_code_f32(float m, int emax) {
+    const uint32_t b = __float_as_uint(m);
+    const int ef = (int)((b >> 23) & 0xFFu);
+    const int e = ef > 0 ? ef - 127 : (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+    return (uint32_t)min(max(e - emax + 127, 0), 254);
+}
+
+__device__ __forceinline__ float mx_multiplier(uint32_t c) {
+    return __uint_as_float((254u - c) << 23);  // 2^(127 - c)
+}
+
 // ------------------------------------------------ deterministic exp / SiLU
 // exp(x): Cody-Waite reduction x = n ln2 + f with ln 2 split into a
 // 16-significant-bit head (45426 / 2^16) and an fp32 tail, the degree-7

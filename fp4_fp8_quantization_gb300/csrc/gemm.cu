@@ -51,7 +51,9 @@ namespace moeq {
 namespace {
 
 enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2, kMxfp4 = 3 };
-enum Epi { kBf16 = 0, kSwiglu = 1 };
+// kSwiglu: SwiGLU + NVFP4 requant; kSwigluMx: SwiGLU + MX requant in the
+// mainloop's element format (MXFP4 -> E2M1, MXFP8 -> E4M3, E8M0 scales).
+enum Epi { kBf16 = 0, kSwiglu = 1, kSwigluMx = 2 };
 
 template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
           int PAIR_, int SF_LOADER_ = 1>
@@ -105,7 +107,10 @@ struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale atoms");
     static_assert(EPI_WARPS % 4 == 0 && COLS_W % 32 == 0 && COLS_W >= 32, "epilogue split");
-    static_assert(ACC_BUFS == 2 || CHUNKS_W <= 4, "single accumulator drains TMEM to registers");
+    static_assert((ACC_BUFS == 2 && EPI == kBf16) || CHUNKS_W <= 4,
+                  "single accumulator / SwiGLU epilogues drain TMEM to registers");
+    static_assert(EPI != kSwigluMx || (CHUNKS_W % 2 == 0 && (KIND == kMxfp4 || KIND == kMxfp8)),
+                  "an MX block is 64 accumulator columns of an MX mainloop");
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
     static_assert(PAIR == 1 || (PAIR == 2 && BN == 256), "a pair splits a 256-row B tile in halves");
 };
@@ -121,6 +126,7 @@ struct Params {
     const uint8_t *a_sf, *b_sf;
     const float *expert_scales;
     const float *out_tensor_scale;
+    const uint16_t *row_scales;  // bf16 per row (SwiGLU + NVFP4), null = 1
     uint16_t *c;
     uint8_t *c_packed, *c_sf;
     uint32_t *err;
@@ -159,7 +165,7 @@ __device__ __forceinline__ uint32_t group_tiles(const Params &p, int g, int NB, 
         return 0;
     }
     uint32_t rows = r1 - r0;
-    if (C::SCALED || EPI == kSwiglu) {
+    if (C::SCALED || EPI != kBf16) {
         uint32_t s0 = __ldg(p.a_sf_offsets + g), s1 = __ldg(p.a_sf_offsets + g + 1);
         uint32_t need = (rows + 127u) & ~127u;
         if ((s0 & 127u) || s1 < s0 || s1 - s0 < need || (int64_t)s1 > p.scale_rows_total) {
@@ -185,11 +191,13 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
 //   bf16 out: c[row, n] = bf16(acc * scale(s)); FP8 rowwise applies
 //             a_scale (rs) then b_scale[e, n]; block-scaled the expert scale.
 //   SwiGLU:   16 (gate, up) pairs -> 16 h -> one NVFP4 block; returns the
-//             E4M3 scale code, writes the 8 packed bytes.
+//             E4M3 scale code, writes the 8 packed bytes.  gate and up are
+//             bf16((acc * s) * rsr): s the expert scale, rsr the row scale
+//             (1 without row scales, an exact no-op).
 template <class C, int KIND, int EPI>
 __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32_t (&r)[32],
                                                    int nc, int e, int64_t row, bool valid,
-                                                   float rs, float inv_out) {
+                                                   float rs, float inv_out, float rsr = 1.0f) {
     if (EPI == kBf16) {
         if (valid) {
 #pragma unroll
@@ -226,13 +234,13 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
         // h = silu(gate) * up with gate, up = bf16(acc * scale), in paired
         // fp32 arithmetic (bit-identical to the scalar definition)
         float h[16];
-        const F2 rs2 = f2(rs, rs);
+        const F2 rs2 = f2(rs, rs), rr2 = f2(rsr, rsr);
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-            const F2 q0 = round_bf16_2(
-                mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2));
-            const F2 q1 = round_bf16_2(
-                mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2));
+            const F2 q0 = round_bf16_2(mul2(
+                mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2), rr2));
+            const F2 q1 = round_bf16_2(mul2(
+                mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2), rr2));
             const F2 hh = swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
             h[i] = f2_lo(hh);
             h[i + 1] = f2_hi(hh);
@@ -293,6 +301,82 @@ __device__ __forceinline__ void copy_stage_scales(uint32_t tmem, const uint8_t *
                                      sdesc_sf_atom(ssfb + 512 * (rb * C::SF_ATOMS + i)));
         }
     }
+}
+
+// SwiGLU + MX requant of 64 accumulator columns (32 (gate, up) pairs, one
+// 32-element MX block) of this thread's row: h as in the NVFP4 epilogue
+// (gate, up = bf16(acc * s)), then the MX rule of the quantizer on the fp32
+// h (scale code from the block amax, elements = elem(h * 2^(127 - c))).
+// Writes 32 (E4M3) or 16 (packed E2M1) bytes; returns the E8M0 code.
+template <int KIND>
+__device__ __forceinline__ uint32_t epilogue_mx_block(const Params &p, const uint32_t (&r0)[32],
+                                                      const uint32_t (&r1)[32], int nc,
+                                                      int64_t row, bool valid, float rs) {
+    float h[32];
+    const F2 rs2 = f2(rs, rs);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint32_t(&r)[32] = half ? r1 : r0;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const F2 q0 = round_bf16_2(
+                mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2));
+            const F2 q1 = round_bf16_2(
+                mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2));
+            const F2 hh = swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
+            h[half * 16 + i] = f2_lo(hh);
+            h[half * 16 + i + 1] = f2_hi(hh);
+        }
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(h[i]));
+    uint32_t code = 0;
+    float f = 0.0f;
+    if (m != 0.0f) {
+        code = mx_scale_code_f32(m, KIND == kMxfp8 ? 8 : 2);
+        f = mx_multiplier(code);
+    }
+    const F2 f2v = f2(f, f);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const F2 t = mul2(f2(h[i], h[i + 1]), f2v);
+        h[i] = f2_lo(t);
+        h[i + 1] = f2_hi(t);
+    }
+    if (valid) {
+        if (KIND == kMxfp8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                w[j] = m == 0.0f ? 0u
+                                 : (e4m3x2(h[4 * j], h[4 * j + 1]) |
+                                    (e4m3x2(h[4 * j + 2], h[4 * j + 3]) << 16));
+            uint8_t *o = p.c_packed + row * (p.N / 2) + nc / 2;
+            st_global_v4(o, w[0], w[1], w[2], w[3]);
+            st_global_v4(o + 16, w[4], w[5], w[6], w[7]);
+        } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float x8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x8[i] = h[8 * j + i];
+                w[j] = m == 0.0f ? 0u : e2m1x8(x8);
+            }
+            st_global_v4(p.c_packed + row * (p.N / 4) + nc / 4, w[0], w[1], w[2], w[3]);
+        }
+    }
+    return code;
+}
+
+// Stores the E8M0 scale byte of the MX block starting at accumulator column
+// nc (output element nc / 2, block nc / 64) of logical scale row prow.
+__device__ __forceinline__ void store_sf_byte_mx(const Params &p, int64_t prow, int nc,
+                                                 uint32_t code) {
+    const int64_t kv_atoms = (p.N / 64 + 3) / 4;
+    const int blk = nc / 64;
+    p.c_sf[sf_word_offset(prow, blk / 4, kv_atoms) + (blk & 3)] = (uint8_t)code;
 }
 
 template <class C, int KIND, int EPI>
@@ -622,6 +706,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 rs = __ldg(p.expert_scales + e);
             }
             if (EPI == kSwiglu) inv_out = __fdiv_rn(1.0f, __ldg(p.out_tensor_scale + e));
+            const float rsr = (EPI == kSwiglu && p.row_scales && valid)
+                                  ? bf16_bits_to_f32(__ldg(p.row_scales + row))
+                                  : 1.0f;
             if (!mbar_wait<PAIRED>(&tfull_bar[buf], aph, abort_v, p.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + lane_off + buf * C::ACC_COLS + cgrp * C::COLS_W;
@@ -634,7 +721,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (lane == 0) release(buf);
                 continue;
             }
-            if (C::ACC_BUFS == 1) {
+            if (C::ACC_BUFS == 1 || EPI != kBf16) {
                 // drain this warp's columns to registers, free TMEM, then compute
                 uint32_t r[C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W][32];
 #pragma unroll
@@ -644,11 +731,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release(buf);
+                if (EPI == kSwigluMx) {
+                    const int64_t prow = (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow;
 #pragma unroll
-                for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
-                    sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
-                                                            valid, rs, inv_out)
-                               << (8 * ch);
+                    for (int b2 = 0; b2 < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W) / 2; ++b2) {
+                        const uint32_t code = epilogue_mx_block<KIND>(
+                            p, r[2 * b2], r[2 * b2 + 1], ncol0 + b2 * 64, row, valid, rs);
+                        if (mb_in_group) store_sf_byte_mx(p, prow, ncol0 + b2 * 64, valid ? code : 0u);
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
+                        sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
+                                                                valid, rs, inv_out, rsr)
+                                   << (8 * ch);
+                }
             } else {
 #pragma unroll 1
                 for (int ch = 0; ch < C::CHUNKS_W; ++ch) {
@@ -660,19 +757,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) release(buf);
                     }
-                    const uint32_t code = epilogue_chunk<C, KIND, EPI>(
-                        p, r, ncol0 + ch * 32, e, row, valid, rs, inv_out);
-                    if (EPI == kSwiglu) {
-                        sfbytes |= code << (8 * (ch & 3));
-                        if ((ch & 3) == 3 && mb_in_group) {
-                            store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow,
-                                           ncol0 + (ch - 3) * 32, valid ? sfbytes : 0u, 4);
-                            sfbytes = 0;
-                        }
-                    }
+                    epilogue_chunk<C, KIND, EPI>(p, r, ncol0 + ch * 32, e, row, valid, rs,
+                                                 inv_out);
                 }
             }
-            if (EPI == kSwiglu && (C::ACC_BUFS == 1 || C::CHUNKS_W < 4) && mb_in_group) {
+            if (EPI == kSwiglu && mb_in_group) {
                 const int nblk = C::CHUNKS_W < 4 ? C::CHUNKS_W : 4;
                 store_sf_bytes(p, (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow, ncol0,
                                valid ? sfbytes : 0u, nblk);
@@ -794,6 +883,7 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     p.b_sf = a.b_sf;
     p.expert_scales = a.expert_scales;
     p.out_tensor_scale = a.out_tensor_scale;
+    p.row_scales = a.row_scales;
     p.c = reinterpret_cast<uint16_t *>(a.c);
     p.c_packed = a.c_packed;
     p.c_sf = a.c_sf;
@@ -896,6 +986,11 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
                         MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
+    if (a.kind == kMxfp4 && a.epi == kSwigluMx)
+        return run_gemm<kMxfp4, kSwigluMx, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
+    if (a.kind == kMxfp8 && a.epi == kSwigluMx)
+        return run_gemm<kMxfp8, kSwigluMx, 128, MOEQ_MX8_STAGES, 2, 8>(a, s);
     if (a.kind == kMxfp4 && a.epi == kBf16)
         return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
                         MOEQ_SF_WARPS, P>(a, s);

@@ -37,12 +37,14 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
 cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_offsets,
                                   int32_t num_groups, cudaStream_t s);
 
-cudaError_t launch_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf, const void *y, int64_t I,
-                                   const float *out_tensor_scale, const GroupArgs &g,
+// out_fmt: 0 NVFP4 (out_tensor_scale required), 1 MXFP4, 2 MXFP8.
+cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, const void *y,
+                                   int64_t I, const float *out_tensor_scale, const GroupArgs &g,
                                    uint32_t *err, cudaStream_t s);
 
 // Grouped GEMMs.  kind: 0 = FP8 rowwise, 1 = NVFP4 block-scaled,
-// 2 = MXFP8 block-scaled.  epi: 0 = bf16 out, 1 = fused SwiGLU + NVFP4.
+// 2 = MXFP8 block-scaled, 3 = MXFP4 block-scaled.  epi: 0 = bf16 out,
+// 1 = fused SwiGLU + NVFP4, 2 = fused SwiGLU + MX in the mainloop's format.
 struct GemmArgs {
     int kind;
     int epi;
@@ -52,7 +54,8 @@ struct GemmArgs {
     const float *a_scales, *b_scales;      // FP8 rowwise
     const uint8_t *a_sf, *b_sf;            // block-scaled
     const float *expert_scales;            // block-scaled (null = 1)
-    const float *out_tensor_scale;         // fused SwiGLU
+    const float *out_tensor_scale;         // fused SwiGLU + NVFP4
+    const uint16_t *row_scales;            // fused SwiGLU + NVFP4: bf16 per row, or null
     void *c;                               // bf16 out
     uint8_t *c_packed, *c_sf;              // fused SwiGLU out
     int32_t max_tokens_per_expert;

@@ -433,24 +433,26 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
 struct SwigluParams {
     const uint16_t *y;   // [T, 2I] bf16
     int64_t I;
-    uint8_t *out;        // [T, I/2]
+    uint8_t *out;        // NVFP4 / MXFP4 [T, I/2], MXFP8 [T, I]
     uint8_t *scales;
-    const float *out_tensor_scale;
+    const float *out_tensor_scale;  // NVFP4 only
     GroupArgs g;
     uint32_t *err;
 };
 
 // One warp per logical scale row; a lane takes 8 (gate, up) pairs = 8 h
-// values per 256-h step, so a 16-h block is held by lanes (2i, 2i+1).
+// values per 256-h step.  OUT: 0 NVFP4 (a 16-h block is held by lanes 2i,
+// 2i+1), 1 MXFP4 / 2 MXFP8 (a 32-h block by lanes 4i .. 4i+3).
+template <int OUT>
 __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
     __shared__ GroupTable table;
-    const GroupView gv = load_groups(p.g, p.out_tensor_scale, table);
+    const GroupView gv = load_groups(p.g, OUT == 0 ? p.out_tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
     const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (prow >= p.g.scale_rows_total) return;
     const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
-    const int64_t kv_atoms = p.I / 64;
+    const int64_t kv_atoms = OUT == 0 ? p.I / 64 : p.I / 128;
     const uint32_t r0 = gv.ro[gi];
     const uint32_t rg = gv.ro[gi + 1] - r0;
     const uint32_t local = (uint32_t)prow - gv.so[gi];
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
         return;
     }
     const int64_t row = (int64_t)r0 + local;
-    const float inv = __fdiv_rn(1.0f, gv.scale(gi));
+    const float inv = OUT == 0 ? __fdiv_rn(1.0f, gv.scale(gi)) : 0.0f;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;
     constexpr int U = 3;  // 256-h steps whose loads are issued together
@@ -500,14 +502,47 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(h[i]));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        Nvfp4Scale s = nvfp4_block_scale(m, inv);
-        uint32_t codes = nvfp4_codes8(h, s.r);
-        uint32_t word = gather4(s.code, lane, 2);
-        if (active) {
-            reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = codes;
-            if ((lane & 7) == 0)
-                *reinterpret_cast<uint32_t *>(
-                    p.scales + sf_word_offset(prow, hl / 64, kv_atoms)) = word;
+        if (OUT == 0) {
+            Nvfp4Scale s = nvfp4_block_scale(m, inv);
+            uint32_t codes = nvfp4_codes8(h, s.r);
+            uint32_t word = gather4(s.code, lane, 2);
+            if (active) {
+                reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = codes;
+                if ((lane & 7) == 0)
+                    *reinterpret_cast<uint32_t *>(
+                        p.scales + sf_word_offset(prow, hl / 64, kv_atoms)) = word;
+            }
+        } else {
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));  // the block's 4 lanes
+            uint32_t code = 0;
+            float f = 0.0f;
+            if (m != 0.0f) {
+                code = mx_scale_code_f32(m, OUT == 2 ? 8 : 2);
+                f = mx_multiplier(code);
+            }
+            float q[8];
+            const F2 f2v = f2(f, f);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const F2 t = mul2(f2(h[i], h[i + 1]), f2v);
+                q[i] = f2_lo(t);
+                q[i + 1] = f2_hi(t);
+            }
+            const uint32_t word = gather4(code, lane, 4);
+            if (active) {
+                if (OUT == 2) {
+                    uint2 o = make_uint2(e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16),
+                                         e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16));
+                    if (m == 0.0f) o = make_uint2(0u, 0u);  // all-zero block: +0 codes
+                    *reinterpret_cast<uint2 *>(p.out + row * p.I + hl) = o;
+                } else {
+                    const uint32_t o = m == 0.0f ? 0u : e2m1x8(q);
+                    reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = o;
+                }
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t *>(
+                        p.scales + sf_word_offset(prow, hl / 128, kv_atoms)) = word;
+            }
         }
       }
     }
@@ -586,14 +621,18 @@ cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_
     return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf, const void *y, int64_t I,
-                                   const float *out_tensor_scale, const GroupArgs &g,
+cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, const void *y,
+                                   int64_t I, const float *out_tensor_scale, const GroupArgs &g,
                                    uint32_t *err, cudaStream_t s) {
-    SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_packed, c_sf, out_tensor_scale,
-                   g, err};
+    SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
     int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks == 0) return cudaSuccess;
-    swiglu_quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    if (out_fmt == 0)
+        swiglu_quantize_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(p);
+    else if (out_fmt == 1)
+        swiglu_quantize_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p);
+    else
+        swiglu_quantize_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

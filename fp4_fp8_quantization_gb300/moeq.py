@@ -36,8 +36,12 @@ _SIGNATURES = {
     "moeq_grouped_matmul_blockscaled": [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                         _I64, _I64, _I32, _I32, _I32, _P],
     "moeq_swiglu_quantize": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P],
-    "moeq_grouped_matmul_swiglu": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
-                                   _I64, _I32, _I32, _I32, _P],
+    "moeq_swiglu_quantize_mx": [_I32, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32,
+                                _P],
+    "moeq_grouped_matmul_swiglu": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                   _I64, _I64, _I32, _I32, _I32, _P],
+    "moeq_grouped_matmul_swiglu_mx": [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                      _I64, _I64, _I32, _I32, _I32, _P],
     "moeq_get_device_error": [_P, _U32P],
     "moeq_clear_device_error": [_P],
     "moeq_last_cuda_error": [],
@@ -198,13 +202,38 @@ def swiglu_quantize(c_packed, c_sf, y, out_tensor_scale, a_offsets, a_scales_off
           _stream(stream))
 
 
+def swiglu_quantize_mx(fmt, c_q, c_sf, y, a_offsets, a_scales_offsets, expert_ids, num_experts,
+                       scale_rows_total, max_tokens_per_expert=0, num_active_experts=None,
+                       stream=None):
+    """Chained SwiGLU + MXFP4 / MXFP8 requantization (fmt "mxfp4" / "mxfp8")."""
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_swiglu_quantize_mx", _fmt(fmt), _ptr(c_q, _U8), _ptr(c_sf, _U8),
+          _ptr(y, torch.bfloat16, "y"), _ptr(a_offsets, _U32), _ptr(a_scales_offsets, _U32),
+          _ptr(expert_ids, torch.int32), y.shape[0], scale_rows_total, y.shape[1] // 2,
+          num_experts, max_tokens_per_expert, G, _stream(stream))
+
+
 def grouped_matmul_swiglu(c_packed, c_sf, a, a_sf, b, b_sf, expert_scales, out_tensor_scale,
                           a_offsets, a_scales_offsets, expert_ids, I, K, scale_rows_total,
-                          max_tokens_per_expert=0, num_active_experts=None, stream=None):
+                          max_tokens_per_expert=0, num_active_experts=None, stream=None,
+                          a_row_scales=None):
     G = expert_ids.numel() if num_active_experts is None else num_active_experts
     _call("moeq_grouped_matmul_swiglu", _ptr(c_packed, _U8), _ptr(c_sf, _U8), _ptr(a, _U8),
           _ptr(a_sf, _U8), _ptr(b, _U8), _ptr(b_sf, _U8), _ptr(expert_scales, torch.float32),
-          _ptr(out_tensor_scale, torch.float32), _ptr(a_offsets, _U32),
+          _ptr(out_tensor_scale, torch.float32),
+          _ptr(a_row_scales, torch.bfloat16, "a_row_scales"), _ptr(a_offsets, _U32),
+          _ptr(a_scales_offsets, _U32), _ptr(expert_ids, torch.int32), a.shape[0],
+          scale_rows_total, I, K, b.shape[0], max_tokens_per_expert, G, _stream(stream))
+
+
+def grouped_matmul_swiglu_mx(fmt, c_q, c_sf, a, a_sf, b, b_sf, expert_scales, a_offsets,
+                             a_scales_offsets, expert_ids, I, K, scale_rows_total,
+                             max_tokens_per_expert=0, num_active_experts=None, stream=None):
+    """Fused grouped MX matmul + SwiGLU + MX requantization (fmt "mxfp4" / "mxfp8")."""
+    G = expert_ids.numel() if num_active_experts is None else num_active_experts
+    _call("moeq_grouped_matmul_swiglu_mx", _fmt(fmt), _ptr(c_q, _U8), _ptr(c_sf, _U8),
+          _ptr(a, _U8), _ptr(a_sf, _U8), _ptr(b, _U8), _ptr(b_sf, _U8),
+          _ptr(expert_scales, torch.float32), _ptr(a_offsets, _U32),
           _ptr(a_scales_offsets, _U32), _ptr(expert_ids, torch.int32), a.shape[0],
           scale_rows_total, I, K, b.shape[0], max_tokens_per_expert, G, _stream(stream))
 

@@ -231,6 +231,27 @@ moeq_status moeq_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf,
                                  int32_t num_active_experts,
                                  moeq_stream_t stream);
 
+/* Chained SwiGLU + MX requantization ("max.nn.moe.NvMxf4f8Strategy": the
+ * strategy handles NVFP4, MXFP4 or MXFP8; fused_silu_quantize applies the
+ * gated activation and then quantizes, read here as quantizing in the
+ * strategy's format; MX formats carry no tensor scale).
+ *   h as in moeq_swiglu_quantize, then per 32-element block of h the MX rule
+ *   of moeq_grouped_quantize: c = clamp(floor(log2 amax) - emax + 127, 0, 254)
+ *   (amax of the fp32 h values), q = elem(h * 2^(127-c)), an all-zero block
+ *   all +0 with c = 0.
+ *   fmt     MOEQ_MXFP4 (E2M1, c_q [total_tokens, I/2] packed) or MOEQ_MXFP8
+ *           (E4M3, c_q [total_tokens, I]).
+ *   c_sf    tiled E8M0 scales [scale_rows_total rows x I/32], padded per
+ *           expert like moeq_grouped_quantize.
+ * I % 128 == 0. */
+moeq_status moeq_swiglu_quantize_mx(moeq_format fmt, uint8_t *c_q, uint8_t *c_sf,
+                                    const void *y, const uint32_t *a_offsets,
+                                    const uint32_t *a_scales_offsets,
+                                    const int32_t *expert_ids, int64_t total_tokens,
+                                    int64_t scale_rows_total, int64_t I,
+                                    int32_t num_experts, int32_t max_tokens_per_expert,
+                                    int32_t num_active_experts, moeq_stream_t stream);
+
 /* Fused grouped NVFP4 matmul + SwiGLU + NVFP4 requantization in one kernel
  * ("max.nn.moe.NvMxf4f8Strategy", grouped_matmul_swiglu: equivalent to
  * grouped_matmul followed by fused_silu_quantize; its (c_packed,
@@ -241,15 +262,37 @@ moeq_status moeq_swiglu_quantize(uint8_t *c_packed, uint8_t *c_sf,
  * and writes the same bytes.  b is [num_experts, 2I, K/2] with gate/up rows
  * interleaved (row 2j = gate_j, row 2j+1 = up_j); b_sf its per-expert tiled
  * scales.  expert_scales and out_tensor_scale are required.
+ *   a_row_scales  optional bf16 [total_tokens] (NULL = none; grouped_matmul_swiglu:
+ *            "BF16 scale per hidden row, applied with the expert scale
+ *            before the SwiGLU"): gate and up become
+ *            bf16((acc * expert_scale) * a_row_scale[t]), two fp32 multiplies
+ *            in that order.  With row scales there is no chained counterpart.
  * K % 256 == 0, I % 64 == 0. */
 moeq_status moeq_grouped_matmul_swiglu(
     uint8_t *c_packed, uint8_t *c_sf, const uint8_t *a, const uint8_t *a_sf,
     const uint8_t *b, const uint8_t *b_sf, const float *expert_scales,
-    const float *out_tensor_scale, const uint32_t *a_offsets,
+    const float *out_tensor_scale, const void *a_row_scales, const uint32_t *a_offsets,
     const uint32_t *a_scales_offsets, const int32_t *expert_ids,
     int64_t total_tokens, int64_t scale_rows_total, int64_t I, int64_t K,
     int32_t num_experts, int32_t max_tokens_per_expert,
     int32_t num_active_experts, moeq_stream_t stream);
+
+/* Fused grouped MX matmul + SwiGLU + MX requantization in one kernel: the
+ * MX counterpart of moeq_grouped_matmul_swiglu (same reading of the
+ * strategy: MXFP4 or MXFP8 throughout).  Computes, with no bf16 tensor in
+ * memory, exactly
+ *   moeq_grouped_matmul_blockscaled(fmt, y, ...) ; moeq_swiglu_quantize_mx(fmt, ..., y, ...)
+ * and writes the same bytes.  a / a_sf / b / b_sf as for
+ * moeq_grouped_matmul_blockscaled(fmt) with N = 2I (gate/up rows of b
+ * interleaved); expert_scales optional (NULL = 1).
+ * MXFP4: K % 256 == 0; MXFP8: K % 128 == 0; I % 128 == 0. */
+moeq_status moeq_grouped_matmul_swiglu_mx(
+    moeq_format fmt, uint8_t *c_q, uint8_t *c_sf, const uint8_t *a, const uint8_t *a_sf,
+    const uint8_t *b, const uint8_t *b_sf, const float *expert_scales,
+    const uint32_t *a_offsets, const uint32_t *a_scales_offsets, const int32_t *expert_ids,
+    int64_t total_tokens, int64_t scale_rows_total, int64_t I, int64_t K,
+    int32_t num_experts, int32_t max_tokens_per_expert, int32_t num_active_experts,
+    moeq_stream_t stream);
 
 /* Reads the sticky device error word of the current device (MOEQ_DEVERR_*
  * bits) after synchronising `stream`.  Returns MOEQ_ERR_DEVICE when any bit

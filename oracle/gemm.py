@@ -75,11 +75,15 @@ def weight_scales_logical(b_sf, E, N, kv):
 
 def grouped_matmul_blockscaled(fmt, a, a_sf, b, b_sf, expert_scales, a_offsets,
                                a_scales_offsets, expert_ids, N, K,
-                               scale_rows_total, out=None, return_f64=False):
+                               scale_rows_total, out=None, return_f64=False,
+                               row_scales=None):
     """a: [T, K/2] packed (NVFP4/MXFP4) or [T, K] (MXFP8); a_sf: flat tiled
     buffer of [scale_rows_total, K/v]; b: [E, N, K/2] or [E, N, K]; b_sf:
     per-expert tiled buffers.  Row t of group g uses scale row
-    a_scales_offsets[g] + (t - a_offsets[g])."""
+    a_scales_offsets[g] + (t - a_offsets[g]).  row_scales (optional, [T]
+    values of bf16 numbers): the per-row scale of grouped_matmul_swiglu
+    ("applied with the expert scale"), multiplied in with the expert scale
+    before the single rounding to bf16."""
     v = 16 if fmt == "nvfp4" else 32
     kv = K // v
     a = np.asarray(a, np.uint8)
@@ -98,6 +102,8 @@ def grouped_matmul_blockscaled(fmt, a, a_sf, b, b_sf, expert_scales, a_offsets,
         acc = deq_a @ deq_b.T
         es = 1.0 if expert_scales is None else float(np.float32(expert_scales[e]))
         val = acc * es
+        if row_scales is not None:
+            val = val * np.asarray(row_scales, np.float64)[r0:r1, None]
         f64[r0:r1] = val
         out[r0:r1] = F.encode_bf16(val)
     return (out, f64) if return_f64 else out

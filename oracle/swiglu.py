@@ -83,13 +83,18 @@ def swiglu(y):
 
 
 def swiglu_quantize(y, out_tensor_scale, a_offsets, a_scales_offsets,
-                    expert_ids, out=None, scales=None, scale_rows_total=None):
-    """Chained SwiGLU + NVFP4 quantization of the bf16 GEMM output y [T, 2I]
-    with the raw per-expert output scale s_e = out_tensor_scale[e].
-    Output: packed [T, I/2] and the tiled scale buffer of [rows, I/16],
-    with the same per-expert padded scale rows as the activations."""
+                    expert_ids, out=None, scales=None, scale_rows_total=None,
+                    fmt="nvfp4"):
+    """Chained SwiGLU + quantization of the bf16 GEMM output y [T, 2I].
+
+    fmt "nvfp4": with the raw per-expert output scale s_e =
+    out_tensor_scale[e]; output packed [T, I/2] and the tiled scale buffer of
+    [rows, I/16].  fmt "mxfp4" / "mxfp8" (the strategy's MX formats, no
+    tensor scale): the MX block rule on the fp32 h values; output [T, I/2]
+    packed E2M1 or [T, I] E4M3 and E8M0 scales of [rows, I/32].  Scale rows
+    are padded per expert as for the activations."""
     h = swiglu(y)
-    return Q.grouped_quantize("nvfp4", h, a_offsets, a_scales_offsets,
-                              expert_ids, tensor_scale=out_tensor_scale,
+    return Q.grouped_quantize(fmt, h, a_offsets, a_scales_offsets, expert_ids,
+                              tensor_scale=out_tensor_scale if fmt == "nvfp4" else None,
                               out=out, scales=scales,
                               scale_rows_total=scale_rows_total)

@@ -88,11 +88,24 @@ def test_gemms_reject_bad_host_arguments(lib):
     a = list(args); a[0] = 2; a[6] = None; a[12] = 192       # N % 128
     assert bs(*a) == 1
     sw = lib.moeq_grouped_matmul_swiglu
-    sargs = [FAKE] * 11 + [64, 128, 64, 512, 2, 8, 2, None]
+    sargs = [FAKE] * 12 + [64, 128, 64, 512, 2, 8, 2, None]
     a = list(sargs); a[7] = None                             # missing SiLU-output scale
     assert sw(*a) == 1
-    a = list(sargs); a[13] = 96                              # I % 64
+    a = list(sargs); a[14] = 96                              # I % 64
     assert sw(*a) == 1
+    a = list(sargs); a[8] = ODD                              # unaligned row scales
+    assert sw(*a) == 1
+    mx = lib.moeq_grouped_matmul_swiglu_mx
+    margs = [1] + [FAKE] * 10 + [64, 128, 128, 512, 2, 8, 2, None]
+    a = list(margs); a[0] = 0                                # NVFP4 is not an MX format
+    assert mx(*a) == 1
+    a = list(margs); a[13] = 64                              # I % 128
+    assert mx(*a) == 1
+    a = list(margs); a[0] = 1; a[14] = 384                   # MXFP4 needs K % 256
+    assert mx(*a) == 1
+    qm = lib.moeq_swiglu_quantize_mx
+    assert qm(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 128, 2, 8, 2, None) == 1
+    assert qm(2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 2, 8, 2, None) == 1
     q = lib.moeq_swiglu_quantize
     assert q(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 64, 128, 64, 2, 8, 2, None) == 1
     assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 2, 8, 2, None) == 1
