@@ -42,10 +42,9 @@ WORKLOAD = ("NVFP4 MoE up-projection: 128 experts, 16384 tokens top-8 uniform ->
 E4, TOK4, TOPK4, K4, I4 = 128, 16384, 8, 4096, 1536
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratios
 FP8_OVER_BF16 = 4.5 / 2.25
-# DRAM bytes (read + write) of one launch of the fused GEMM on this workload
-# from one ncu capture of the current kernel; None until the kernel as built
-# now has been captured.
-FUSED_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) of one launch of the fused GEMM on this workload,
+# from one ncu capture of the current kernel (1.21 GB read + 109.5 MB written).
+FUSED_TRAFFIC_BYTES = 1.3195e9
 
 
 def parse_args():
@@ -316,6 +315,34 @@ def parts(pk, flush):
     return out
 
 
+def mx_part(d, pk):
+    """The up-projection in MXFP4 throughout on the same workload: MXFP4
+    quantize of the activations, then the fused MXFP4 GEMM + SwiGLU + MXFP4
+    requant (E8M0 block-32 scales; random weights and weight scales)."""
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    T, N, rows = d["T"], d["N"], d["rows"]
+    a = torch.empty_like(d["a"])
+    asf = torch.empty(moeq.sf_bytes(rows, K4 // 32), dtype=torch.uint8, device="cuda")
+    b = synth.random_fp4_packed((E4, N, K4 // 2), seed=501, device="cuda")
+    bsf = synth.random_bytes(E4 * moeq.sf_bytes(N, K4 // 32), 116, 126, seed=502, device="cuda")
+    c = torch.empty((T, I4 // 2), dtype=torch.uint8, device="cuda")
+    csf = torch.empty(moeq.sf_bytes(rows, I4 // 32), dtype=torch.uint8, device="cuda")
+
+    def quant():
+        moeq.grouped_quantize("mxfp4", d["x"], a, asf, d["ro"], d["so"], d["ids"], None, E4, rows)
+
+    def fused():
+        moeq.grouped_matmul_swiglu_mx("mxfp4", c, csf, a, asf, b, bsf, d["es"], d["ro"], d["so"],
+                                      d["ids"], I4, K4, rows, d["mt"])
+
+    t_q = time_kernel(quant, 10)
+    t_f = time_kernel(fused, 10)
+    fl = flops_up(d)
+    return {"quantize_mxfp4_ms": round(t_q, 4), "fused_gemm_swiglu_mxfp4_ms": round(t_f, 4),
+            "fused_TFLOP/s": round(fl / t_f / 1e9, 1),
+            "fused_frac_fp4_peak": round(fl / t_f / 1e9 / (pk["bf16"] * FP4_OVER_BF16), 4)}
+
+
 def chained_part(d, pk):
     from fp4_fp8_quantization_gb300 import moeq
     y = torch.empty((d["T"], d["N"]), dtype=torch.bfloat16, device="cuda")
@@ -572,6 +599,7 @@ def run_moeq(args, rank, world):
     extra = {}
     if rank == 0 and not args.no_parts:
         extra["chained_same_workload"] = chained_part(d, pk)
+        extra["mxfp4_same_workload"] = mx_part(d, pk)
         extra["moe_layer_same_workload"] = layer_part(d)
         extra.update(parts(pk, None))
     err = moeq.get_device_error()
