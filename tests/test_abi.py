@@ -103,6 +103,8 @@ def test_gemms_reject_bad_host_arguments(lib):
     assert mx(*a) == 1
     a = list(margs); a[0] = 1; a[14] = 384                   # MXFP4 needs K % 256
     assert mx(*a) == 1
+    a = list(args); a[0] = 0; a[16] = 1025                  # more groups than the scheduler
+    assert bs(*a) == 2
     qm = lib.moeq_swiglu_quantize_mx
     assert qm(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 128, 2, 8, 2, None) == 1
     assert qm(2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 64, 2, 8, 2, None) == 1
