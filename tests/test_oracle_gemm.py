@@ -89,8 +89,9 @@ def test_fp8_rowwise_brute_force_exact():
     assert np.all(out[~written] == 0xBEEF)
 
 
-@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8", "mxfp4"])
-def test_blockscaled_brute_force_exact(fmt):
+@pytest.mark.parametrize("fmt,with_rows", [("nvfp4", False), ("nvfp4", True), ("mxfp8", False),
+                                           ("mxfp4", False)])
+def test_blockscaled_brute_force_exact(fmt, with_rows):
     rng = np.random.default_rng(21)
     v = 16 if fmt == "nvfp4" else 32
     E, N, K = 3, 4, 64
@@ -124,8 +125,10 @@ def test_blockscaled_brute_force_exact(fmt):
         es = None
     a_sf = L.swizzle(sa_log)
     b_sf = np.concatenate([L.swizzle(sb_log[e]) for e in range(E)])
+    # optional per-row scales (bf16 values): multiply in with the expert scale
+    rs = F.round_bf16(rng.uniform(0.5, 2.0, T)).astype(np.float64) if with_rows else None
     out = G.grouped_matmul_blockscaled(fmt, a, a_sf, b, b_sf, es, ro, so, ids,
-                                       N=N, K=K, scale_rows_total=rows)
+                                       N=N, K=K, scale_rows_total=rows, row_scales=rs)
     for g in range(len(counts)):
         e = int(ids[g])
         for i, t in enumerate(range(int(ro[g]), int(ro[g + 1]))):
@@ -136,6 +139,8 @@ def test_blockscaled_brute_force_exact(fmt):
                           for k in range(K))
                 if es is not None:
                     acc *= Fraction(float(es[e]))
+                if rs is not None:
+                    acc *= Fraction(float(rs[t]))
                 assert out[t, n] == F.encode_bf16(float(acc)), (t, n)
 
 

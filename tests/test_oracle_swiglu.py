@@ -58,6 +58,25 @@ def test_swiglu_worked_blocks():
         assert np.array_equal(q[0], np.array(body[3].split(), np.uint8)), name
 
 
+def test_swiglu_mx_worked_blocks():
+    """swiglu_quantize in the MX formats on one-row groups, against the
+    hand-worked blocks (element codes before packing and the E8M0 code)."""
+    for name, attrs, _, body in cases("swiglu_mx_blocks.txt", 4):
+        fmt = attrs["fmt"]
+        gate = np.array(body[0].split(), np.float32)
+        up = np.array(body[1].split(), np.float32)
+        y = np.empty((1, 64), np.float32)
+        y[0, 0::2] = gate
+        y[0, 1::2] = up
+        ro = np.array([0, 1], np.uint32)
+        so = np.array([0, 128], np.uint32)
+        out, sf = S.swiglu_quantize(y, None, ro, so, np.array([0], np.int32), fmt=fmt)
+        codes = np.array([int(c, 16) for c in body[3].split()], np.uint8)
+        got = out[0] if fmt == "mxfp8" else F.unpack_e2m1(out[0:1])[0]
+        assert np.array_equal(got, codes), name
+        assert int(L.unswizzle(sf, 128, 1)[0, 0]) == int(body[2].split()[1], 16), name
+
+
 def test_swiglu_gate_up_order():
     # gate = 1, up = 3  ->  silu(1) * 3;  swapping would give silu(3) * 1
     h = S.swiglu(np.array([[1.0, 3.0]], np.float32))[0, 0]
