@@ -13,7 +13,10 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoeq.so")
+# The in-tree library, or another build of it named by MOEQ_LIB (e.g. one
+# compiled with different tile options by build.build(variant_dir, flags)).
+_LIB_PATH = os.environ.get("MOEQ_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libmoeq.so")
 _lib = None
 
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
