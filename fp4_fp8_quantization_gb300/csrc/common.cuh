@@ -177,91 +177,72 @@ __device__ __forceinline__ float mx_multiplier(uint32_t c) {
 }
 
 // ------------------------------------------------ deterministic exp / SiLU
-// exp(x): Cody-Waite reduction x = n ln2 + f with ln 2 split into a
-// 16-significant-bit head (45426 / 2^16) and an fp32 tail, the degree-7
-// Taylor polynomial of e^f by Horner's rule with separately rounded
-// multiplies and adds, then two exact power-of-two multiplies by 2^(n/2).
-// x >= 89 gives +inf, x <= -104 gives 0.  The same steps are the library's
-// definition of the SwiGLU activation, so results are reproducible bit for bit.
-__device__ __forceinline__ float exp_spec(float x) {
+// The library's SiLU, silu(g) = g * sigma(g), is defined by the steps below,
+// each one IEEE fp32 operation or one fused multiply-add (a single
+// rounding), so that every kernel reproduces it bit for bit:
+//   e     = exp(-|g|): Cody-Waite reduction x = n ln2 + f with ln 2 split
+//           into a 16-significant-bit head (45426 / 2^16) and an fp32 tail,
+//           the degree-7 Taylor polynomial of e^f by Horner's rule, then
+//           p * 2^n with 2^n taken as 0 for n < -126 (x clamped to >= -104);
+//   d     = 1 + e, in [1, 2];
+//   r     = 1 / d: Newton-Raphson from the minimax line 24/17 - 8/17 d,
+//           three steps q = 1 - d r, r = r + r q;
+//   sigma = r for g >= 0, e * r otherwise (e / (1 + e) = 1 / (1 + e^-g)).
+// All of it runs two values at a time in paired arithmetic.
+
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+    F2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return d;
+}
+
+__device__ __forceinline__ F2 f2s(float x) { return f2(x, x); }
+
+// e^x of two arguments x <= 0 (a NaN argument gives 0).
+__device__ __forceinline__ F2 exp_neg2(float x0, float x1) {
     const float kLog2e = 1.44269502162933349609375f;      // fp32(1 / ln 2)
     const float kLn2Hi = 0.693145751953125f;              // 45426 / 65536
     const float kLn2Lo = 1.428606765330187045037746429443359375e-06f;
-    const float c0 = 1.0f, c1 = 1.0f, c2 = 0.5f;
-    const float c3 = 0.16666667163372039794921875f;      // fp32(1/3!)
-    const float c4 = 0.0416666679084300994873046875f;    // fp32(1/4!)
-    const float c5 = 0.008333333767950534820556640625f;  // fp32(1/5!)
-    const float c6 = 0.001388888922519981861114501953125f;    // fp32(1/6!)
-    const float c7 = 0.0001984127011382952332496643066406f;   // fp32(1/7!)
-    // Branch-free: evaluate on the clamped argument, select the limits after.
-    const float xc = fminf(fmaxf(x, -104.0f), 89.0f);
-    float n = rintf(__fmul_rn(xc, kLog2e));
-    float f = __fsub_rn(xc, __fmul_rn(n, kLn2Hi));
-    f = __fsub_rn(f, __fmul_rn(n, kLn2Lo));
-    float p = c7;
-    p = __fadd_rn(__fmul_rn(p, f), c6);
-    p = __fadd_rn(__fmul_rn(p, f), c5);
-    p = __fadd_rn(__fmul_rn(p, f), c4);
-    p = __fadd_rn(__fmul_rn(p, f), c3);
-    p = __fadd_rn(__fmul_rn(p, f), c2);
-    p = __fadd_rn(__fmul_rn(p, f), c1);
-    p = __fadd_rn(__fmul_rn(p, f), c0);
-    int ni = (int)n;
-    int n1 = ni >> 1;                     // floor(n / 2)
-    int n2 = ni - n1;
-    float s1 = __int_as_float((n1 + 127) << 23);
-    float s2 = __int_as_float((n2 + 127) << 23);
-    float r = __fmul_rn(__fmul_rn(p, s1), s2);
-    r = (x >= 89.0f) ? __int_as_float(0x7f800000) : r;
-    return (x <= -104.0f) ? 0.0f : r;
-}
-
-__device__ __forceinline__ float silu_spec(float g) {
-    return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
-}
-
-// exp_spec of two arguments, the same steps in paired arithmetic: each
-// result equals exp_spec of its argument bit for bit.
-__device__ __forceinline__ F2 exp_spec2(float x0, float x1) {
-    const F2 kLog2e = f2(1.44269502162933349609375f, 1.44269502162933349609375f);
-    const F2 kLn2Hi = f2(0.693145751953125f, 0.693145751953125f);
-    const F2 kLn2Lo = f2(1.428606765330187045037746429443359375e-06f,
-                         1.428606765330187045037746429443359375e-06f);
-    const float c[8] = {1.0f, 1.0f, 0.5f, 0.16666667163372039794921875f,
-                        0.0416666679084300994873046875f, 0.008333333767950534820556640625f,
-                        0.001388888922519981861114501953125f,
-                        0.0001984127011382952332496643066406f};
-    const float xc0 = fminf(fmaxf(x0, -104.0f), 89.0f);
-    const float xc1 = fminf(fmaxf(x1, -104.0f), 89.0f);
-    const F2 xc = f2(xc0, xc1);
-    const F2 t = mul2(xc, kLog2e);
-    const float n0 = rintf(f2_lo(t)), n1 = rintf(f2_hi(t));
-    const F2 n = f2(n0, n1);
-    F2 f = sub2(xc, mul2(n, kLn2Hi));
-    f = sub2(f, mul2(n, kLn2Lo));
-    F2 p = f2(c[7], c[7]);
+    const float kShift = 12582912.0f;                     // 1.5 * 2^23
+    const float c[8] = {1.0f, 1.0f, 0.5f,
+                        0.16666667163372039794921875f,          // fp32(1/3!)
+                        0.0416666679084300994873046875f,        // fp32(1/4!)
+                        0.008333333767950534820556640625f,      // fp32(1/5!)
+                        0.001388888922519981861114501953125f,   // fp32(1/6!)
+                        0.0001984127011382952332496643066406f}; // fp32(1/7!)
+    const F2 xc = f2(fmaxf(x0, -104.0f), fmaxf(x1, -104.0f));
+    // t = 1.5 * 2^23 + n, n = x log2(e) rounded to an integer (ties to even)
+    const F2 t = fma2(xc, f2s(kLog2e), f2s(kShift));
+    const F2 n = sub2(t, f2s(kShift));
+    F2 f = fma2(n, f2s(-kLn2Hi), xc);
+    f = fma2(n, f2s(-kLn2Lo), f);
+    F2 p = f2s(c[7]);
 #pragma unroll
-    for (int k = 6; k >= 0; --k) p = add2(mul2(p, f), f2(c[k], c[k]));
-    const int i0 = (int)n0, i1 = (int)n1;
-    const int a0 = i0 >> 1, a1 = i1 >> 1;
-    const F2 s1 = f2(__int_as_float((a0 + 127) << 23), __int_as_float((a1 + 127) << 23));
-    const F2 s2 = f2(__int_as_float((i0 - a0 + 127) << 23), __int_as_float((i1 - a1 + 127) << 23));
-    const F2 r = mul2(mul2(p, s1), s2);
-    float r0 = f2_lo(r), r1 = f2_hi(r);
-    r0 = (x0 >= 89.0f) ? __int_as_float(0x7f800000) : r0;
-    r1 = (x1 >= 89.0f) ? __int_as_float(0x7f800000) : r1;
-    return f2((x0 <= -104.0f) ? 0.0f : r0, (x1 <= -104.0f) ? 0.0f : r1);
+    for (int k = 6; k >= 0; --k) p = fma2(p, f, f2s(c[k]));
+    // the bits of t are 0x4B400000 + n (n in [-150, 0]): shifted left by 23
+    // they give the exponent field n (mod 2^32); the fp32 bits of 2^n are
+    // (n + 127) << 23, negative (then clamped to +0) for n < -126
+    const int s0 = max((int)((__float_as_uint(f2_lo(t)) << 23) + (127u << 23)), 0);
+    const int s1 = max((int)((__float_as_uint(f2_hi(t)) << 23) + (127u << 23)), 0);
+    return mul2(p, f2(__int_as_float(s0), __int_as_float(s1)));
 }
 
-// h = silu_spec(g) * u for two (gate, up) pairs, bit-identical to the
-// scalar steps.
+// h = silu(g) * u for two (gate, up) pairs.
 __device__ __forceinline__ F2 swiglu2(float g0, float g1, float u0, float u1) {
-    const F2 den = add2(f2(1.0f, 1.0f), exp_spec2(-g0, -g1));
-    const F2 sl = f2(__fdiv_rn(g0, f2_lo(den)), __fdiv_rn(g1, f2_hi(den)));
-    return mul2(sl, f2(u0, u1));
+    const float kSeedA = 1.41176474094390869140625f;      // fp32(24 / 17)
+    const float kSeedB = 0.4705882370471954345703125f;    // fp32(8 / 17)
+    const F2 e = exp_neg2(-fabsf(g0), -fabsf(g1));
+    const F2 nd = sub2(f2s(-1.0f), e);                    // -d = -(1 + e)
+    F2 r = fma2(nd, f2s(kSeedB), f2s(kSeedA));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const F2 q = fma2(nd, r, f2s(1.0f));
+        r = fma2(r, q, r);
+    }
+    const F2 er = mul2(e, r);
+    const F2 sg = f2(g0 >= 0.0f ? f2_lo(r) : f2_lo(er), g1 >= 0.0f ? f2_hi(r) : f2_hi(er));
+    return mul2(mul2(f2(g0, g1), sg), f2(u0, u1));
 }
-
-
 
 // ----------------------------------------------------- tiled scale layout
 // Byte offset of the 4-byte word holding scale columns [4 kb, 4 kb + 4) of

@@ -1,6 +1,10 @@
-"""Pins of the oracle's exp / SiLU definition (against long-double exp and
-limits fixed by the mathematics) and of the chained SwiGLU requantization
-(hand-worked blocks, gate/up order, grouping)."""
+"""Pins of the oracle's exp / reciprocal / SiLU definition (its fused
+multiply-add against exact rational arithmetic, accuracy against long-double
+exp and float64 SiLU, limits fixed by the mathematics) and of the chained
+SwiGLU requantization (hand-worked blocks, gate/up order, grouping)."""
+import math
+from fractions import Fraction
+
 import numpy as np
 
 from oracle import formats as F
@@ -10,39 +14,125 @@ from oracle import swiglu as S
 from tests._golden import cases
 
 
-def test_exp_spec_accuracy_vs_long_double():
-    x = np.concatenate([np.linspace(-87.0, 88.5, 400001),
-                        F.decode_bf16(np.arange(0x0000, 0x42B0, 7)),
-                        -F.decode_bf16(np.arange(0x0000, 0x42AE, 7))]).astype(np.float32)
-    got = S.exp_spec(x).astype(np.longdouble)
+def _round_f32_exact(q):
+    """Nearest-even fp32 value of the exact rational q (as a Python float),
+    written from the definition: the quantum 2^(e - 23) of q's binade
+    (subnormal binade below 2^-126), round half to even, overflow to inf."""
+    if q == 0:
+        return 0.0
+    sign = -1.0 if q < 0 else 1.0
+    q = abs(q)
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    m = q / quantum
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    v = fl * quantum
+    if v >= Fraction(2) ** 128:
+        return sign * math.inf
+    return sign * float(v)
+
+
+def test_fma_f32_double_rounding_case():
+    """a * b + c = 0.75 + 2^-25 + 2^-61: just above the midpoint between
+    0.75 and 0.75 + 2^-24.  Rounding the float64 sum to nearest first lands
+    on the midpoint (and then on 0.75); one rounding gives 0.75 + 2^-24."""
+    a = np.float32((1 + 2.0 ** -12) * 2.0 ** -25)
+    b = np.float32(1 - 2.0 ** -12 + 2.0 ** -24)
+    c = np.float32(0.75)
+    assert float(a) * float(b) == 2.0 ** -25 + 2.0 ** -61
+    assert np.float32(np.float64(a) * np.float64(b) + np.float64(c)) == 0.75
+    assert S.fma_f32(a, b, c) == np.float32(0.75 + 2.0 ** -24)
+
+
+def test_fma_f32_against_exact_rationals():
+    rng = np.random.default_rng(41)
+    n = 3000
+    a = (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n)).astype(np.float32)
+    b = (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n)).astype(np.float32)
+    c = (rng.standard_normal(n) * 2.0 ** rng.integers(-60, 60, n)).astype(np.float32)
+    # cancellation: c close to -a*b
+    k = n // 3
+    c[:k] = -(a[:k].astype(np.float64) * b[:k]).astype(np.float32)
+    c[k:2 * k] = np.nextafter(c[:k], np.float32(np.inf))
+    # subnormal and tiny results
+    a[-50:] = np.float32(2.0 ** -75)
+    b[-50:] = rng.uniform(0.5, 1.0, 50).astype(np.float32) * np.float32(2.0 ** -60)
+    c[-50:] = np.float32(0.0)
+    got = S.fma_f32(a, b, c)
+    for i in range(n):
+        exact = Fraction(float(a[i])) * Fraction(float(b[i])) + Fraction(float(c[i]))
+        assert float(got[i]) == _round_f32_exact(exact), (i, a[i], b[i], c[i])
+
+
+def test_exp_neg_spec_accuracy_vs_long_double():
+    x = np.concatenate([np.linspace(-87.0, 0.0, 400001),
+                        -F.decode_bf16(np.arange(0x0000, 0x42AE, 3))]).astype(np.float32)
+    got = S.exp_neg_spec(x).astype(np.longdouble)
     ref = np.exp(x.astype(np.longdouble))
     rel = np.abs(got - ref) / ref
-    assert rel.max() <= 2.0 ** -21, float(rel.max())
+    assert rel.max() <= 2.0 ** -22, float(rel.max())
 
 
-def test_exp_spec_special_points():
-    assert S.exp_spec(np.float32(0.0)) == 1.0
-    assert np.isinf(S.exp_spec(np.float32(89.0)))
-    assert np.isinf(S.exp_spec(np.float32(88.8)))          # overflows naturally
-    assert np.isfinite(S.exp_spec(np.float32(88.7)))
-    assert S.exp_spec(np.float32(-104.0)) == 0.0
-    # subnormal results: within one subnormal step of the true value
-    for x in (-90.0, -100.0, -103.0):
-        got = float(S.exp_spec(np.float32(x)))
-        assert abs(got - np.exp(x)) <= 2.0 ** -149
+def test_exp_neg_spec_special_points():
+    assert S.exp_neg_spec(np.float32(0.0)) == 1.0
+    assert S.exp_neg_spec(np.float32(-0.0)) == 1.0
+    assert S.exp_neg_spec(np.float32(-104.0)) == 0.0
+    assert S.exp_neg_spec(np.float32(-1e30)) == 0.0
+    assert S.exp_neg_spec(np.float32(-np.inf)) == 0.0
+    assert S.exp_neg_spec(np.float32(np.nan)) == 0.0
+    # 2^n below 2^-126 is taken as 0: x log2(e) = -126.52 rounds to n = -127
+    assert S.exp_neg_spec(np.float32(-87.7)) == 0.0
+    # n = -126: a normal result close to e^x
+    v = float(S.exp_neg_spec(np.float32(-87.3)))
+    assert v >= 2.0 ** -126 and abs(v - math.exp(float(np.float32(-87.3)))) / v < 2.0 ** -22
+
+
+def test_recip_spec_accuracy():
+    d = np.arange(0x3F800000, 0x40000001, 3, dtype=np.uint32).view(np.float32)
+    d = np.concatenate([d, np.float32([1.0, 1.5, 2.0])])
+    r = S.recip_spec(d).astype(np.float64)
+    ref = 1.0 / d.astype(np.float64)
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(r - ref) / ulp) <= 0.51
+    assert S.recip_spec(np.float32(1.0)) == 1.0
+    assert S.recip_spec(np.float32(2.0)) == 0.5
 
 
 def test_silu_limits():
-    assert S.silu_spec(np.float32(0.0)) == 0.0
+    z = S.silu_spec(np.float32(0.0))
+    assert z == 0.0 and not np.signbit(z)
+    z = S.silu_spec(np.float32(-0.0))
+    assert z == 0.0 and np.signbit(z)
     assert S.silu_spec(np.float32(32.0)) == 32.0
     assert S.silu_spec(np.float32(1000.0)) == 1000.0
+    assert S.silu_spec(np.float32(np.inf)) == np.inf
+    assert np.isnan(S.silu_spec(np.float32(np.nan)))
     r = S.silu_spec(np.float32(-200.0))
     assert r == 0.0 and np.signbit(r)
     g = np.linspace(-60, 60, 20001).astype(np.float32)
     ref = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64)))
     got = S.silu_spec(g).astype(np.float64)
     big = np.abs(ref) > 1e-30
-    assert np.max(np.abs(got[big] - ref[big]) / np.abs(ref[big])) < 2.0 ** -20
+    assert np.max(np.abs(got[big] - ref[big]) / np.abs(ref[big])) < 2.0 ** -21
+
+
+def test_silu_every_bf16_input():
+    """Every finite bf16 gate value (the fused and chained paths feed SiLU
+    bf16 numbers): within 2^-21 relative of float64 SiLU wherever that is
+    above 1e-30, and -0 / 0 below (e^-|g| under 2^-126 is flushed)."""
+    g = F.decode_bf16(np.arange(0, 65536)).astype(np.float32)
+    g = g[np.isfinite(g)]
+    got = S.silu_spec(g).astype(np.float64)
+    with np.errstate(over="ignore"):
+        ref = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64)))
+    big = np.abs(ref) > 1e-30
+    assert np.max(np.abs(got[big] - ref[big]) / np.abs(ref[big])) < 2.0 ** -21
+    assert np.all(np.abs(got[~big]) <= 1e-30)
 
 
 def test_swiglu_worked_blocks():
