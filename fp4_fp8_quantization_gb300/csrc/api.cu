@@ -98,6 +98,40 @@ moeq_status moeq_padded_scale_offsets(const uint32_t *row_offsets, uint32_t *sca
         moeq::launch_padded_offsets(row_offsets, scales_offsets, num_active_experts, stream));
 }
 
+// Sizes of the layout helpers: products stay far below 2^62.
+static bool layout_sizes_ok(int64_t batch, int64_t rows, int64_t cols) {
+    const int64_t lim = (int64_t)1 << 40;
+    return batch >= 0 && rows >= 0 && cols >= 0 && batch < lim && rows < lim && cols < lim &&
+           (batch == 0 || rows == 0 || cols == 0 ||
+            (double)batch * (double)(rows + 128) * (double)(cols + 4) < 4e18);
+}
+
+moeq_status moeq_sf_swizzle(uint8_t *tiled, const uint8_t *logical, int64_t batch, int64_t rows,
+                            int64_t kv, moeq_stream_t stream) {
+    if (!layout_sizes_ok(batch, rows, kv)) return MOEQ_ERR_INVALID_ARG;
+    if (batch == 0 || rows == 0 || kv == 0) return MOEQ_OK;
+    if (!tiled || !logical) return MOEQ_ERR_INVALID_ARG;
+    return cuda_status(moeq::launch_sf_swizzle(tiled, logical, batch, rows, kv, stream));
+}
+
+moeq_status moeq_sf_unswizzle(uint8_t *logical, const uint8_t *tiled, int64_t batch,
+                              int64_t rows, int64_t kv, moeq_stream_t stream) {
+    if (!layout_sizes_ok(batch, rows, kv)) return MOEQ_ERR_INVALID_ARG;
+    if (batch == 0 || rows == 0 || kv == 0) return MOEQ_OK;
+    if (!tiled || !logical) return MOEQ_ERR_INVALID_ARG;
+    return cuda_status(moeq::launch_sf_unswizzle(logical, tiled, batch, rows, kv, stream));
+}
+
+moeq_status moeq_interleave_gate_up(uint8_t *out, const uint8_t *gate, const uint8_t *up,
+                                    int64_t batch, int64_t rows, int64_t row_bytes,
+                                    moeq_stream_t stream) {
+    if (!layout_sizes_ok(batch, 2 * rows, row_bytes)) return MOEQ_ERR_INVALID_ARG;
+    if (batch == 0 || rows == 0 || row_bytes == 0) return MOEQ_OK;
+    if (!out || !gate || !up) return MOEQ_ERR_INVALID_ARG;
+    return cuda_status(
+        moeq::launch_interleave_rows(out, gate, up, batch, rows, row_bytes, stream));
+}
+
 static moeq_status amax_impl(const void *in, int64_t in_row_stride, int64_t total_rows,
                              int64_t K, const uint32_t *row_offsets, const int32_t *expert_ids,
                              float *tensor_scale_out, int32_t num_experts,

@@ -42,6 +42,15 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
                                    int64_t I, const float *out_tensor_scale, const GroupArgs &g,
                                    uint32_t *err, cudaStream_t s);
 
+// Weight-preparation layout kernels (layout.cu).
+cudaError_t launch_sf_swizzle(uint8_t *tiled, const uint8_t *logical, int64_t batch, int64_t rows,
+                              int64_t kv, cudaStream_t s);
+cudaError_t launch_sf_unswizzle(uint8_t *logical, const uint8_t *tiled, int64_t batch,
+                                int64_t rows, int64_t kv, cudaStream_t s);
+cudaError_t launch_interleave_rows(uint8_t *out, const uint8_t *gate, const uint8_t *up,
+                                   int64_t batch, int64_t rows, int64_t row_bytes,
+                                   cudaStream_t s);
+
 // Grouped GEMMs.  kind: 0 = FP8 rowwise, 1 = NVFP4 block-scaled,
 // 2 = MXFP8 block-scaled, 3 = MXFP4 block-scaled.  epi: 0 = bf16 out,
 // 1 = fused SwiGLU + NVFP4, 2 = fused SwiGLU + MX in the mainloop's format.

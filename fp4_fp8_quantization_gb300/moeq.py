@@ -45,6 +45,9 @@ _SIGNATURES = {
                                    _I64, _I64, _I32, _I32, _I32, _P],
     "moeq_grouped_matmul_swiglu_mx": [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                       _I64, _I64, _I32, _I32, _I32, _P],
+    "moeq_sf_swizzle": [_P, _P, _I64, _I64, _I64, _P],
+    "moeq_sf_unswizzle": [_P, _P, _I64, _I64, _I64, _P],
+    "moeq_interleave_gate_up": [_P, _P, _P, _I64, _I64, _I64, _P],
     "moeq_get_device_error": [_P, _U32P],
     "moeq_clear_device_error": [_P],
     "moeq_last_cuda_error": [],
@@ -171,6 +174,38 @@ def padded_scale_offsets(row_offsets, scales_offsets, num_active_experts=None, s
     G = row_offsets.numel() - 1 if num_active_experts is None else num_active_experts
     _call("moeq_padded_scale_offsets", _ptr(row_offsets, _U32), _ptr(scales_offsets, _U32), G,
           _stream(stream))
+
+
+def sf_swizzle(tiled, logical, stream=None):
+    """logical uint8 [rows, kv] or [batch, rows, kv] -> the tiled block-scale
+    layout in `tiled` (uint8, batch * sf_bytes(rows, kv) bytes)."""
+    batch, rows, kv = (1, *logical.shape) if logical.dim() == 2 else logical.shape
+    if tiled.numel() != batch * sf_bytes(rows, kv):
+        raise ValueError("tiled: expected batch * sf_bytes(rows, kv) bytes")
+    _call("moeq_sf_swizzle", _ptr(tiled, _U8, "tiled"), _ptr(logical, _U8, "logical"), batch,
+          rows, kv, _stream(stream))
+
+
+def sf_unswizzle(logical, tiled, stream=None):
+    """The inverse of sf_swizzle: fills logical uint8 [rows, kv] or
+    [batch, rows, kv] from the tiled buffer."""
+    batch, rows, kv = (1, *logical.shape) if logical.dim() == 2 else logical.shape
+    if tiled.numel() != batch * sf_bytes(rows, kv):
+        raise ValueError("tiled: expected batch * sf_bytes(rows, kv) bytes")
+    _call("moeq_sf_unswizzle", _ptr(logical, _U8, "logical"), _ptr(tiled, _U8, "tiled"), batch,
+          rows, kv, _stream(stream))
+
+
+def interleave_gate_up(out, gate, up, stream=None):
+    """out[b, 2j] = gate[b, j], out[b, 2j + 1] = up[b, j]: uint8 gate, up
+    [batch, rows, row_bytes] (or 2-D), out [batch, 2 * rows, row_bytes]."""
+    if gate.shape != up.shape:
+        raise ValueError("gate and up must have the same shape")
+    batch, rows, rb = (1, *gate.shape) if gate.dim() == 2 else gate.shape
+    if out.numel() != batch * 2 * rows * rb:
+        raise ValueError("out: expected batch * 2 * rows * row_bytes bytes")
+    _call("moeq_interleave_gate_up", _ptr(out, _U8, "out"), _ptr(gate, _U8, "gate"),
+          _ptr(up, _U8, "up"), batch, rows, rb, _stream(stream))
 
 
 def grouped_matmul_rowwise_fp8(c, a, b, a_scales, b_scales, a_offsets, expert_ids,

@@ -294,6 +294,40 @@ moeq_status moeq_grouped_matmul_swiglu_mx(
     int32_t num_experts, int32_t max_tokens_per_expert, int32_t num_active_experts,
     moeq_stream_t stream);
 
+/* ---- weight preparation ("max.nn.moe.NvMxf4f8Strategy", prepare_weight_scales:
+ * "interleaves NVIDIA block scales for kernel layout").  Run once per weight,
+ * off the per-step path.  Every pointer is a caller-owned device pointer;
+ * the calls only enqueue work on `stream`.  batch, rows, kv / row_bytes == 0
+ * is MOEQ_OK and a no-op; negative sizes or NULL pointers (with a non-empty
+ * call) return MOEQ_ERR_INVALID_ARG before any launch. */
+
+/* Logical -> tiled block-scale layout, for `batch` independent matrices
+ * (e.g. one per expert).
+ *   logical  uint8 [batch, rows, kv], row-major, kv = K / block size
+ *   tiled    uint8 [batch, ceil(rows / 128) * ceil(kv / 4) * 512]: matrix b starts at byte
+ *            b * ceil(rows / 128) * ceil(kv / 4) * 512; inside it scale (r, c)
+ *            sits in the 512-byte atom (r / 128, c / 4) (atoms row-block-major)
+ *            at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4 -- the layout
+ *            every block-scaled call reads and writes.
+ * Bytes of the tiled buffer that hold no logical scale are written 0. */
+moeq_status moeq_sf_swizzle(uint8_t *tiled, const uint8_t *logical, int64_t batch,
+                            int64_t rows, int64_t kv, moeq_stream_t stream);
+
+/* Tiled -> logical (the inverse of moeq_sf_swizzle; padding is not read
+ * into the output, which holds exactly batch * rows * kv bytes). */
+moeq_status moeq_sf_unswizzle(uint8_t *logical, const uint8_t *tiled, int64_t batch,
+                              int64_t rows, int64_t kv, moeq_stream_t stream);
+
+/* Gate/up interleave of the fused SwiGLU GEMM's weight: out[b, 2j, :] =
+ * gate[b, j, :] and out[b, 2j + 1, :] = up[b, j, :] for rows of row_bytes
+ * bytes (packed weight rows, K / 2 bytes for E2M1; or logical scale rows,
+ * kv bytes, then moeq_sf_swizzle with 2 * rows rows).
+ *   gate, up uint8 [batch, rows, row_bytes];  out uint8 [batch, 2 * rows, row_bytes]
+ * out must not overlap the inputs. */
+moeq_status moeq_interleave_gate_up(uint8_t *out, const uint8_t *gate, const uint8_t *up,
+                                    int64_t batch, int64_t rows, int64_t row_bytes,
+                                    moeq_stream_t stream);
+
 /* Reads the sticky device error word of the current device (MOEQ_DEVERR_*
  * bits) after synchronising `stream`.  Returns MOEQ_ERR_DEVICE when any bit
  * is set, MOEQ_OK otherwise. */

@@ -58,3 +58,18 @@ def unswizzle(buf, rows, kv):
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
     rr, cc = np.meshgrid(np.arange(rows), np.arange(kv), indexing="ij")
     return buf[sf_offset(rr, cc, kv)]
+
+
+def interleave_rows(gate, up):
+    """Gate/up interleave of the fused SwiGLU weight ([..., rows, cols] ->
+    [..., 2 rows, cols]): row 2j is gate row j, row 2j+1 is up row j.  The
+    reading of "max.nn.moe.NvMxf4f8Strategy" adopted for the gate/up
+    arrangement (granularity-1 interleave), applied to weight rows and to
+    their logical block-scale rows alike."""
+    gate = np.asarray(gate)
+    up = np.asarray(up)
+    assert gate.shape == up.shape
+    out = np.empty(gate.shape[:-2] + (2 * gate.shape[-2], gate.shape[-1]), gate.dtype)
+    out[..., 0::2, :] = gate
+    out[..., 1::2, :] = up
+    return out

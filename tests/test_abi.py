@@ -67,6 +67,21 @@ def test_quantize_rejects_bad_host_arguments(lib):
     assert call(fmt=2, ts=None, G=0) == 0  # MX needs no tensor scale
 
 
+def test_layout_helpers_reject_bad_host_arguments(lib):
+    sw, un, il = lib.moeq_sf_swizzle, lib.moeq_sf_unswizzle, lib.moeq_interleave_gate_up
+    for f in (sw, un):
+        assert f(FAKE, FAKE, -1, 128, 4, None) == 1    # negative sizes
+        assert f(FAKE, FAKE, 1, -5, 4, None) == 1
+        assert f(None, FAKE, 1, 128, 4, None) == 1     # NULL with work to do
+        assert f(FAKE, None, 1, 128, 4, None) == 1
+        assert f(None, None, 0, 128, 4, None) == 0     # empty: OK, nothing launched
+        assert f(None, None, 3, 0, 4, None) == 0
+        assert f(FAKE, FAKE, 1 << 41, 128, 4, None) == 1   # beyond the size limit
+    assert il(FAKE, FAKE, FAKE, 1, -1, 16, None) == 1
+    assert il(FAKE, None, FAKE, 1, 4, 16, None) == 1
+    assert il(None, None, None, 2, 4, 0, None) == 0
+
+
 def test_gemms_reject_bad_host_arguments(lib):
     r = lib.moeq_grouped_matmul_rowwise_fp8
     #        c     a     b     sa    sb    ao    ids   T   N    K    E  mt  G  stream

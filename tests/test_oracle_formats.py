@@ -134,3 +134,11 @@ def test_sf_layout_is_a_bijection_and_roundtrips():
             mask = np.ones(buf.size, bool)
             mask[offs] = False
             assert not buf[mask].any()
+
+
+def test_interleave_rows_hand_case():
+    gate = np.array([[[1, 2], [3, 4]], [[9, 10], [11, 12]]], np.uint8)
+    up = np.array([[[5, 6], [7, 8]], [[13, 14], [15, 16]]], np.uint8)
+    want = np.array([[[1, 2], [5, 6], [3, 4], [7, 8]],
+                     [[9, 10], [13, 14], [11, 12], [15, 16]]], np.uint8)
+    assert np.array_equal(L.interleave_rows(gate, up), want)
