@@ -397,6 +397,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
                  : "memory");
 }
 
+// Arrival without memory ordering, for an accumulator release: the arriving
+// warp's tensor-memory loads have completed (tcgen05.wait::ld) before it
+// arrives, and the waiter needs nothing else from it.  A release at cluster
+// scope would first wait for every global store the warp has in flight.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
