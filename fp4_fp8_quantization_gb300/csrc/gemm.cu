@@ -507,6 +507,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     sfb0 = ((int64_t)e * nrb + n0 / 128) * kv_atoms;
                     rbs = min(C::RB, nrb - n0 / 128);
                 }
+                if (PAIRED) rbs = C::RB;  // one box of RB row blocks (see below)
                 const uint32_t tx =
                     (do_ab ? (uint32_t)(C::A_BYTES + C::B_BYTES) : 0u) +
                     (do_sf ? (uint32_t)(C::SFA_BYTES + rbs * C::SF_ATOMS * C::SF_ATOM_BYTES) : 0u);
@@ -546,11 +547,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             // atom is two rows
                             tma_load_2d_pair(ssfa, &tmSFA, fb, 0,
                                              (int)((sfa0 + (int64_t)kt * C::SF_ATOMS) * 2), pol_a);
-                            for (int rb = 0; rb < rbs; ++rb)
-                                tma_load_2d_pair(
-                                    ssfb + rb * C::SF_ATOMS * 512, &tmSFB, fb, 0,
-                                    (int)((sfb0 + rb * kv_atoms + (int64_t)kt * C::SF_ATOMS) * 2),
-                                    pol_b);
+                            // all RB row blocks of B scales in one copy (a row
+                            // block past the expert's N reads the next
+                            // expert's or zero-filled rows, never used)
+                            tma_load_3d_pair(ssfb, &tmSFB, fb, 0, kt * C::SF_ATOMS * 2,
+                                             e * nrb + n0 / 128, pol_b);
                         }
                     }
                     issued |= 1u << stage;
@@ -832,6 +833,24 @@ bool make_flat_map(CUtensorMap *m, const void *base, int64_t bytes, cuuint32_t b
     return r == CUDA_SUCCESS;
 }
 
+// uint8 tensor map over the B scales viewed as [row blocks][2 kv_atoms rows
+// of 256 bytes] (no swizzle): boxes of box_rows rows of box_rb consecutive
+// row blocks, so one copy brings a stage's scale atoms of every B row block
+// of a tile.
+bool make_sfb_map(CUtensorMap *m, const void *base, int64_t row_blocks, int64_t kv_atoms,
+                  cuuint32_t box_rows, cuuint32_t box_rb) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {256, (cuuint64_t)(2 * kv_atoms), (cuuint64_t)row_blocks};
+    cuuint64_t strides[2] = {256, (cuuint64_t)(kv_atoms * 512)};
+    cuuint32_t box[3] = {256, box_rows, box_rb};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cache[64] = {0};
     int dev = 0;
@@ -866,7 +885,9 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
         const int64_t sfa_bytes = a.groups.scale_rows_total / 128 * kv_atoms * 512;
         const int64_t sfb_bytes = E * ((a.N + 127) / 128) * kv_atoms * 512;
         if (!make_flat_map(&tSFA, a.a_sf, sfa_bytes, 2 * C::SF_ATOMS)) return cudaErrorInvalidValue;
-        if (!make_flat_map(&tSFB, a.b_sf, sfb_bytes, 2 * C::SF_ATOMS)) return cudaErrorInvalidValue;
+        if (!make_sfb_map(&tSFB, a.b_sf, E * ((a.N + 127) / 128), kv_atoms, 2 * C::SF_ATOMS, C::RB))
+            return cudaErrorInvalidValue;
+        (void)sfb_bytes;
     }
     Params p;
     p.a_offsets = a.groups.row_offsets;
