@@ -206,26 +206,34 @@ def flops_up(d):
 
 # ------------------------------------------------------------ sub-parts
 
-def time_kernel(fn, iters, flush=None, warmup=3):
-    """Mean device time (ms) of one call.  `fn` is a callable or a list of
+def time_kernel(fn, iters, flush=None, warmup=3, batch=1):
+    """Device time (ms) of one call.  `fn` is a callable or a list of
     callables used in rotation (input sets whose total exceeds L2, so every
     call reads from HBM); an L2 flush (write of a buffer larger than L2)
-    precedes every timed call when `flush` is given."""
+    precedes every timed call when `flush` is given.  With batch > 1 the
+    events bracket `batch` back-to-back calls (the launch of one overlaps
+    the end of the previous) and the median over `iters` batches of the
+    per-call time is returned; otherwise the mean over `iters` single
+    calls."""
     fns = fn if isinstance(fn, (list, tuple)) else [fn]
-    for i in range(warmup):
+    for i in range(max(warmup, 2 * batch)):
         fns[i % len(fns)]()
     ts = []
+    k = 0
     for i in range(iters):
         if flush is not None:
             flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        fns[i % len(fns)]()
+        for _ in range(batch):
+            fns[k % len(fns)]()
+            k += 1
         e1.record()
         ts.append((e0, e1))
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+    per = [a.elapsed_time(b) / batch for a, b in ts]
+    return statistics.median(per) if batch > 1 else statistics.mean(per)
 
 
 def parts(pk, flush):
@@ -250,19 +258,22 @@ def parts(pk, flush):
     so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
     moeq.padded_scale_offsets(ro_d, so_d)
     ts = torch.empty(8, device=dev)
+    # batches of 8 back-to-back calls over the rotating sets (20 batches)
     t_amax = time_kernel([lambda x=x: moeq.grouped_amax_scale(x, ro_d, ids_d, ts, 8) for x in xs],
-                         20)
+                         20, batch=8)
     for fmt, ob, v in (("nvfp4", 2048, 16), ("mxfp8", 4096, 32)):
         qs = [torch.empty((T, ob), dtype=torch.uint8, device=dev) for _ in range(NSET)]
         sfs = [torch.empty(moeq.sf_bytes(rows, 4096 // v), dtype=torch.uint8, device=dev)
                for _ in range(NSET)]
         ms = time_kernel([lambda x=x, q=q, sf=sf, fmt=fmt: moeq.grouped_quantize(
-            fmt, x, q, sf, ro_d, so_d, ids_d, ts, 8, rows) for x, q, sf in zip(xs, qs, sfs)], 20)
+            fmt, x, q, sf, ro_d, so_d, ids_d, ts, 8, rows) for x, q, sf in zip(xs, qs, sfs)], 20,
+            batch=8)
         nbytes = T * 4096 * 2 + qs[0].numel() + sfs[0].numel()
         out[f"quantize_{fmt}_8192x4096"] = {
             "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
             "frac_hbm": round(nbytes / ms / 1e6 / hbm, 4), "bytes": nbytes,
-            "l2": "4 rotating input sets (268 MB > L2)"}
+            "l2": "4 rotating input sets (268 MB > L2)",
+            "timing": "median over 20 batches of 8 back-to-back calls"}
     out["amax_8192x4096"] = {"ms": round(t_amax, 5),
                              "GB/s": round(T * 4096 * 2 / t_amax / 1e6, 1),
                              "frac_hbm": round(T * 4096 * 2 / t_amax / 1e6 / hbm, 4)}
