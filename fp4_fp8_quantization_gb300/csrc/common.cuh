@@ -342,6 +342,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Waits for a phase with a bound but without consulting the abort flag;
+// used only to drain in-flight asynchronous work before the CTA exits.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    uint32_t a = smem_u32(bar);
+    long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) break;
+    }
+}
+
 // TMA tiled loads into this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y, uint64_t policy) {

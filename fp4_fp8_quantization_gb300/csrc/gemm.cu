@@ -178,16 +178,6 @@ __device__ __forceinline__ uint32_t group_tiles(const Params &p, int g, int NB, 
     return ((rows + C::BM - 1) / C::BM + C::PAIR - 1) / C::PAIR * (uint32_t)NB;
 }
 
-// Waits for a phase with a bound but without consulting the abort flag;
-// used only to drain in-flight asynchronous work before the CTA exits.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    uint32_t a = smem_u32(bar);
-    long long t0 = clock64();
-    while (!mbar_try_wait(a, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) break;
-    }
-}
-
 // Epilogue of one 32-column accumulator chunk of this thread's row.
 //   bf16 out: c[row, n] = bf16(acc * scale(s)); FP8 rowwise applies
 //             a_scale (rs) then b_scale[e, n]; block-scaled the expert scale.
