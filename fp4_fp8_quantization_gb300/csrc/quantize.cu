@@ -18,10 +18,6 @@ namespace moeq {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-// 32-byte loads in flight per lane in the quantizer's row loop.
-#ifndef MOEQ_QUANT_U
-#define MOEQ_QUANT_U 4
-#endif
 
 // The group description, read either from a per-CTA shared-memory copy
 // (up to kTableCap groups: one coalesced round trip per CTA instead of a
@@ -115,22 +111,8 @@ __device__ __forceinline__ int scale_row_group(const GroupView &g, uint32_t p, u
     return group_ok(g, gi, err, true) ? gi : -1;
 }
 
-// Maps data row t to its group: returns g, or -1 when t lies in no group
-// (or the group is invalid; flag_bad_groups reports those).
-__device__ __forceinline__ int row_group(const GroupView &g, uint32_t t) {
-    const int G = g.G;
-    if (G <= 0 || t < g.ro[0] || t >= g.ro[G]) return -1;
-    const int gi = find_group(g.ro, G, t);
-    if (t < g.ro[gi] || t >= g.ro[gi + 1]) return -1;  // non-monotone offsets
-    return group_ok(g, gi, nullptr, true) ? gi : -1;
-}
-
-// Sets the error bits of every invalid group (one CTA calls it).
-__device__ __forceinline__ void flag_bad_groups(const GroupView &g, uint32_t *err) {
-    for (int i = threadIdx.x; i < g.G; i += blockDim.x) group_ok(g, i, err, true);
-}
-
-// The same without scale rows (the amax pass takes none).
+// Sets the error bits of every invalid group without scale rows (one CTA
+// calls it; the amax pass takes no scale offsets).
 __device__ __forceinline__ void flag_bad_groups_rows(const GroupView &g, uint32_t *err) {
     for (int i = threadIdx.x; i < g.G; i += blockDim.x) group_ok(g, i, err, false);
 }
@@ -328,34 +310,24 @@ __device__ __forceinline__ void load_step(const uint8_t *a, uint32_t (&w)[8]) {
 // [16 i, 16 i + 16) of each 512-element step, a whole block.  Codes go to
 // out_row, the E4M3 block scales to logical scale row prow.  r_tab[c] =
 // inv / value(c) for every E4M3 code c (0 where the block scale is 0).
-// Loads steps [s0, s0 + U) of a row (lane i: bytes [32 i, 32 i + 32) of
-// each 1024-byte step); steps past the row and idle lanes of the last step
-// read nothing and give zeros.
-template <bool A32, int U>
-__device__ __forceinline__ void load_batch(const uint8_t *src, int s0, int nsteps, int lanes_last,
-                                           int lane, uint32_t (&w)[U][8]) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[u][i] = 0u;
-        const int s = s0 + u;
-        if (src && s < nsteps && (s < nsteps - 1 || lane < lanes_last))
-            load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
-    }
-}
-
 template <bool A32>
 __device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *out_row,
                                                    uint8_t *scales, int64_t prow, int64_t K,
-                                                   float inv, const float *r_tab, int lane,
-                                                   uint32_t (&w)[MOEQ_QUANT_U][8]) {
+                                                   float inv, const float *r_tab, int lane) {
     const int64_t kv_atoms = K / 64;
     const int nsteps = (int)((K + 511) / 512);
     const int lanes_last = (int)(K / 16 - (int64_t)(nsteps - 1) * 32);
-    constexpr int U = MOEQ_QUANT_U;
+    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
     for (int s0 = 0; s0 < nsteps; s0 += U) {
-        // the first batch arrives loaded
-        if (s0 > 0) load_batch<A32, U>(src, s0, nsteps, lanes_last, lane, w);
+        uint32_t w[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            const int s = s0 + u;
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int s = s0 + u;
@@ -395,40 +367,29 @@ __device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
 // 512-element step lane i takes elements [16 i, 16 i + 16): a whole NVFP4
 // block, or half of an MX block (lanes 2j, 2j+1 share block j).
 template <int FMT, bool A32>
-__global__ void __launch_bounds__(256, 4) quantize_kernel(QuantParams p) {
+__global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
     __shared__ float r_table[kWarpsPerCta][128];
     __shared__ GroupTable table;
+    const GroupView gv = load_groups(p.g, FMT == 0 ? p.tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    // one warp per data row; its first loads go out before the group table
-    // is read, so the two memory round trips overlap
-    const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + wid;
-    const bool in_range = row < p.g.total_rows;
-    const int64_t srow = in_range ? source_row(p.gt, row, nullptr) : -1;
-    const uint8_t *src =
-        srow >= 0 ? reinterpret_cast<const uint8_t *>(p.in + srow * p.stride) : nullptr;
-    constexpr int U = MOEQ_QUANT_U;
-    const int nsteps = (int)((p.K + 511) / 512);
-    const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
-    uint32_t w[U][8];
-    load_batch<A32, U>(src, 0, nsteps, lanes_last, lane, w);
-    const GroupView gv = load_groups(p.g, FMT == 0 ? p.tensor_scale : nullptr, table);
-    if (blockIdx.x == 0) flag_bad_groups(gv, p.err);
-    if (!in_range) return;
-    const int gi = row_group(gv, (uint32_t)row);
+    const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + wid;
+    if (prow >= p.g.scale_rows_total) return;
+    const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
-    if (!src) {  // gathered index outside the input: flag it, skip the row
-        set_error(p.err, MOEQ_DEVERR_BAD_INDEX);
-        return;
-    }
     constexpr int V = FMT == 0 ? 16 : 32;
     const int64_t kv_atoms = p.K / V / 4;
-    const uint32_t rg = gv.ro[gi + 1] - gv.ro[gi];
-    const uint32_t local = (uint32_t)row - gv.ro[gi];
-    const int64_t prow = (int64_t)gv.so[gi] + local;
-    // the group's padding scale rows [rg, ceil128(rg)), dealt over its rows
-    for (uint32_t q = rg + local; q < ((rg + 127u) & ~127u); q += rg)
-        zero_scale_row(p.scales, (int64_t)gv.so[gi] + q, kv_atoms, lane);
+    const uint32_t r0 = gv.ro[gi];
+    const uint32_t rg = gv.ro[gi + 1] - r0;
+    const uint32_t local = (uint32_t)prow - gv.so[gi];
+    if (local >= rg) {  // padding row of this group (up to the next multiple of 128)
+        if (local < ((rg + 127u) & ~127u)) zero_scale_row(p.scales, prow, kv_atoms, lane);
+        return;
+    }
+    const int64_t row = (int64_t)r0 + local;
+    const int64_t srow = source_row(p.gt, row, p.err);  // gathered input row
+    if (srow < 0) return;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + srow * p.stride);
     if (FMT == 0) {
         // r depends only on the block's E4M3 scale code: tabulate
         // r[c] = inv / value(c) once per row (same IEEE division per entry).
@@ -437,11 +398,22 @@ __global__ void __launch_bounds__(256, 4) quantize_kernel(QuantParams p) {
         for (int j = 0; j < 4; ++j) r_table[wid][lane * 4 + j] = nvfp4_r_entry(lane * 4 + j, inv);
         __syncwarp();
         nvfp4_quantize_row<A32>(src, p.out + row * (p.K / 2), p.scales, prow, p.K, inv,
-                                r_table[wid], lane, w);
+                                r_table[wid], lane);
         return;
     }
+    const int nsteps = (int)((p.K + 511) / 512);
+    const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
+    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
     for (int s0 = 0; s0 < nsteps; s0 += U) {
-        if (s0 > 0) load_batch<A32, U>(src, s0, nsteps, lanes_last, lane, w);
+        uint32_t w[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            const int s = s0 + u;
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int s = s0 + u;
@@ -663,8 +635,7 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
                             const Gather &gt, uint32_t *err, cudaStream_t s) {
     QuantParams p{reinterpret_cast<const uint16_t *>(in), stride, K, out, scales, tensor_scale,
                   g, gt, err};
-    // one warp per data row (padding scale rows are written by their group's rows)
-    int64_t blocks = (g.total_rows + kWarpsPerCta - 1) / kWarpsPerCta;
+    int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks == 0) return cudaSuccess;
     // 256-bit loads need every row start 32-byte aligned
     const bool a32 = (reinterpret_cast<uintptr_t>(in) % 32 == 0) && (stride % 16 == 0);
