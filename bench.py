@@ -279,6 +279,21 @@ def parts(pk, flush):
                              "frac_hbm": round(T * 4096 * 2 / t_amax / 1e6 / hbm, 4)}
     del xs
 
+    # tiny FP8 rowwise: E 4, groups of 7 / 16 / 9 rows on experts 2 / 0 / 3,
+    # K 128, N 64 (a latency figure: one launch, back to back)
+    ro_t = np.array([0, 7, 23, 32], np.uint32)
+    ids_t = np.array([2, 0, 3], np.int32)
+    a_t = synth.e4m3_normal((32, 128), 1.0, seed=40, device=dev)
+    b_t = synth.e4m3_normal((4, 64, 128), 0.5, seed=41, device=dev)
+    sa_t = synth.uniform((32,), 0.01, 0.1, seed=42, device=dev)
+    sb_t = synth.uniform((4, 64), 0.005, 0.05, seed=43, device=dev)
+    c_t = torch.empty((32, 64), dtype=torch.bfloat16, device=dev)
+    ro_td, ids_td = u32(ro_t), torch.from_numpy(ids_t).to(dev)
+    ms = time_kernel(lambda: moeq.grouped_matmul_rowwise_fp8(c_t, a_t, b_t, sa_t, sb_t, ro_td,
+                                                             ids_td, 16), 20, batch=8)
+    out["fp8_rowwise_tiny_32x64x128"] = {"us": round(ms * 1e3, 2),
+                                         "timing": "median over 20 batches of 8 back-to-back calls"}
+
     # FP8 rowwise at MoE scale: 64 experts, 8192 tokens top-8 Zipf(1.1), K 7168, N 4096
     counts = synth.routing_counts(8192, 8, 64, seed=0, zipf_s=1.1)
     ro, ids = synth.ragged_groups(counts)

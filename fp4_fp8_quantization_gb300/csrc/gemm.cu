@@ -904,9 +904,21 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     // upper bound of the tiles (pair tiles for PAIR > 1) the offsets can give
     const int64_t tiles_ub = (T / (C::BM * PAIR) + a.groups.num_groups) * nb;
     auto kern = grouped_gemm_kernel<C, KIND, EPI>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    // per-device launch set-up of this kernel, done once (the shared-memory
+    // attribute and, for pairs, the resident cluster count); concurrent
+    // first calls only repeat the same idempotent queries
+    static int attr_done[64] = {0};
+    static int max_cl_cache[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = 1;
+    }
     if (PAIR == 1) {
         const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
         kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, tSFA, tSFB, p);
@@ -925,10 +937,13 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(sm_count() / PAIR * PAIR), 1, 1);
-    int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorNotSupported;
+    int max_clusters = max_cl_cache[dev];
+    if (!max_clusters) {
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (max_clusters < 1) return cudaErrorNotSupported;
+        max_cl_cache[dev] = max_clusters;
+    }
     int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * PAIR), 1, 1);
     e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSFA, tSFB, p);

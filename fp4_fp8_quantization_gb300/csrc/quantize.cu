@@ -18,6 +18,21 @@ namespace moeq {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
+// Quantizer launch shape: warps per CTA, 32-byte loads in flight per lane,
+// minimum resident CTAs per SM (which caps the registers).  CTAs of 4 warps,
+// 4 loads per lane, at most 64 registers (8 CTAs per SM): against 8-warp
+// CTAs with 62-72 registers, 9 % faster on 8192 x 4096 and 12 % on
+// 131072 x 4096 rows (same box, back-to-back calls).
+#ifndef MOEQ_Q_WARPS
+#define MOEQ_Q_WARPS 4
+#endif
+#ifndef MOEQ_QUANT_U
+#define MOEQ_QUANT_U 4
+#endif
+#ifndef MOEQ_Q_MINB
+#define MOEQ_Q_MINB 8
+#endif
+constexpr int kQWarps = MOEQ_Q_WARPS;
 
 // The group description, read either from a per-CTA shared-memory copy
 // (up to kTableCap groups: one coalesced round trip per CTA instead of a
@@ -317,7 +332,7 @@ __device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *
     const int64_t kv_atoms = K / 64;
     const int nsteps = (int)((K + 511) / 512);
     const int lanes_last = (int)(K / 16 - (int64_t)(nsteps - 1) * 32);
-    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
+    constexpr int U = MOEQ_QUANT_U;  // 32-byte loads in flight per lane
     for (int s0 = 0; s0 < nsteps; s0 += U) {
         uint32_t w[U][8];
 #pragma unroll
@@ -367,13 +382,13 @@ __device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
 // 512-element step lane i takes elements [16 i, 16 i + 16): a whole NVFP4
 // block, or half of an MX block (lanes 2j, 2j+1 share block j).
 template <int FMT, bool A32>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
-    __shared__ float r_table[kWarpsPerCta][128];
+__global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB) quantize_kernel(QuantParams p) {
+    __shared__ float r_table[kQWarps][128];
     __shared__ GroupTable table;
     const GroupView gv = load_groups(p.g, FMT == 0 ? p.tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + wid;
+    const int64_t prow = (int64_t)blockIdx.x * kQWarps + wid;
     if (prow >= p.g.scale_rows_total) return;
     const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
@@ -403,7 +418,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantParams p) {
     }
     const int nsteps = (int)((p.K + 511) / 512);
     const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
-    constexpr int U = 4;  // 4 x 32 bytes in flight per lane
+    constexpr int U = MOEQ_QUANT_U;  // 32-byte loads in flight per lane
     for (int s0 = 0; s0 < nsteps; s0 += U) {
         uint32_t w[U][8];
 #pragma unroll
@@ -635,19 +650,19 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
                             const Gather &gt, uint32_t *err, cudaStream_t s) {
     QuantParams p{reinterpret_cast<const uint16_t *>(in), stride, K, out, scales, tensor_scale,
                   g, gt, err};
-    int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
+    int64_t blocks = (g.scale_rows_total + kQWarps - 1) / kQWarps;
     if (blocks == 0) return cudaSuccess;
     // 256-bit loads need every row start 32-byte aligned
     const bool a32 = (reinterpret_cast<uintptr_t>(in) % 32 == 0) && (stride % 16 == 0);
     if (fmt == 0)
-        a32 ? quantize_kernel<0, true><<<(unsigned)blocks, 256, 0, s>>>(p)
-            : quantize_kernel<0, false><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<0, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
+            : quantize_kernel<0, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
     else if (fmt == 1)
-        a32 ? quantize_kernel<1, true><<<(unsigned)blocks, 256, 0, s>>>(p)
-            : quantize_kernel<1, false><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<1, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
+            : quantize_kernel<1, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
     else
-        a32 ? quantize_kernel<2, true><<<(unsigned)blocks, 256, 0, s>>>(p)
-            : quantize_kernel<2, false><<<(unsigned)blocks, 256, 0, s>>>(p);
+        a32 ? quantize_kernel<2, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
+            : quantize_kernel<2, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
