@@ -17,7 +17,6 @@ namespace moeq {
 
 namespace {
 
-constexpr int kWarpsPerCta = 8;
 // Quantizer launch shape: warps per CTA, 32-byte loads in flight per lane,
 // minimum resident CTAs per SM (which caps the registers).  CTAs of 4 warps,
 // 4 loads per lane, at most 64 registers (8 CTAs per SM): against 8-warp
@@ -33,6 +32,30 @@ constexpr int kWarpsPerCta = 8;
 #define MOEQ_Q_MINB 8
 #endif
 constexpr int kQWarps = MOEQ_Q_WARPS;
+// amax pass: warps per CTA, rows per warp on large inputs (>= 65536 rows:
+// 2 is 2 % faster than 4 on 131072 x 4096), min CTAs per SM
+#ifndef MOEQ_A_WARPS
+#define MOEQ_A_WARPS 8
+#endif
+#ifndef MOEQ_A_RPW
+#define MOEQ_A_RPW 2
+#endif
+#ifndef MOEQ_A_MINB
+#define MOEQ_A_MINB 1
+#endif
+// chained SwiGLU: warps per CTA, 256-h steps in flight, min CTAs per SM.
+// 4-warp CTAs, two steps, at most 48 registers (10 CTAs per SM): 23 % faster
+// than 8-warp CTAs, three steps and 92 registers on 131072 x 3072.
+#ifndef MOEQ_S_WARPS
+#define MOEQ_S_WARPS 4
+#endif
+#ifndef MOEQ_S_U
+#define MOEQ_S_U 2
+#endif
+#ifndef MOEQ_S_MINB
+#define MOEQ_S_MINB 10
+#endif
+constexpr int kSWarps = MOEQ_S_WARPS;
 
 // The group description, read either from a per-CTA shared-memory copy
 // (up to kTableCap groups: one coalesced round trip per CTA instead of a
@@ -215,7 +238,7 @@ __device__ __forceinline__ uint32_t row_abs_max(const uint4 *src, int64_t K, int
     return __reduce_max_sync(0xFFFFFFFFu, m);
 }
 
-__global__ void __launch_bounds__(256) amax_kernel(const uint16_t *__restrict__ in,
+__global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(const uint16_t *__restrict__ in,
                                                    int64_t stride, int64_t K, GroupArgs g,
                                                    Gather gt,
                                                    uint32_t *__restrict__ amax_bits,
@@ -495,11 +518,11 @@ struct SwigluParams {
 // values per 256-h step.  OUT: 0 NVFP4 (a 16-h block is held by lanes 2i,
 // 2i+1), 1 MXFP4 / 2 MXFP8 (a 32-h block by lanes 4i .. 4i+3).
 template <int OUT>
-__global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
+__global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_kernel(SwigluParams p) {
     __shared__ GroupTable table;
     const GroupView gv = load_groups(p.g, OUT == 0 ? p.out_tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
-    const int64_t prow = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    const int64_t prow = (int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5);
     if (prow >= p.g.scale_rows_total) return;
     const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
@@ -515,7 +538,7 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
     const float inv = OUT == 0 ? __fdiv_rn(1.0f, gv.scale(gi)) : 0.0f;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;
-    constexpr int U = 3;  // 256-h steps whose loads are issued together
+    constexpr int U = MOEQ_S_U;  // 256-h steps whose loads are issued together
     for (int64_t hb = 0; hb < nh; hb += 256 * U) {
       uint4 v[U][2];
 #pragma unroll
@@ -633,10 +656,10 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
     if (e != cudaSuccess) return e;
     if (g.total_rows > 0) {
         // enough warps to fill the GPU on small inputs, 4 rows each on large
-        const int rows_per_warp = g.total_rows >= 65536 ? 4 : 1;
+        const int rows_per_warp = g.total_rows >= 65536 ? MOEQ_A_RPW : 1;
         int64_t warps = (g.total_rows + rows_per_warp - 1) / rows_per_warp;
-        int64_t blocks = (warps + 7) / 8;
-        amax_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+        int64_t blocks = (warps + MOEQ_A_WARPS - 1) / MOEQ_A_WARPS;
+        amax_kernel<<<(unsigned)blocks, MOEQ_A_WARPS * 32, 0, s>>>(
             reinterpret_cast<const uint16_t *>(in), stride, K, g, gt,
             reinterpret_cast<uint32_t *>(tensor_scale_out), err, rows_per_warp);
     }
@@ -676,14 +699,14 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
                                    int64_t I, const float *out_tensor_scale, const GroupArgs &g,
                                    uint32_t *err, cudaStream_t s) {
     SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
-    int64_t blocks = (g.scale_rows_total + kWarpsPerCta - 1) / kWarpsPerCta;
+    int64_t blocks = (g.scale_rows_total + kSWarps - 1) / kSWarps;
     if (blocks == 0) return cudaSuccess;
     if (out_fmt == 0)
-        swiglu_quantize_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(p);
+        swiglu_quantize_kernel<0><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
     else if (out_fmt == 1)
-        swiglu_quantize_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p);
+        swiglu_quantize_kernel<1><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
     else
-        swiglu_quantize_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(p);
+        swiglu_quantize_kernel<2><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
