@@ -510,13 +510,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     uint8_t *sb = sa + C::A_BYTES;
                     uint8_t *ssfa = sb + C::B_BYTES;
                     uint8_t *ssfb = ssfa + C::SFA_BYTES;
+                    bool stuck = false;
+#ifdef MOEQ_TEST_STUCK_STAGE
+                    // failure-detection test build: the first stage of the
+                    // CTA's first tile is announced but never loaded, so every
+                    // wait on it runs into its time limit
+                    stuck = !PAIRED && t == cid && kt == 0;
+#endif
                     if (!PAIRED) {
                         mbar_arrive_expect_tx(&full_bar[stage], tx);
-                        if (do_ab) {
+                        if (do_ab && !stuck) {
                             tma_load_2d(sa, &tmA, &full_bar[stage], kt * C::BK_BYTES, row0, pol_a);
                             tma_load_3d(sb, &tmB, &full_bar[stage], kt * C::BK_BYTES, n0, e, pol_b);
                         }
-                        if (do_sf) {
+                        if (do_sf && !stuck) {
                             bulk_load(ssfa, p.a_sf + (sfa0 + (int64_t)kt * C::SF_ATOMS) * 512,
                                       C::SFA_BYTES, &full_bar[stage]);
                             for (int rb = 0; rb < rbs; ++rb)
@@ -544,8 +551,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                              e * nrb + n0 / 128, pol_b);
                         }
                     }
-                    issued |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (!stuck) {
+                        issued |= 1u << stage;
+                        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
