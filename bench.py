@@ -518,11 +518,13 @@ def run_moeq(args, rank, world):
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("moeq timed steps")   # one range around the timed region
     start.record()
     for i in range(args.steps):
         up_projection_step(d, evs[i])
     end.record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     ms_total = start.elapsed_time(end)
     clk = clocks.stop()
