@@ -8,33 +8,37 @@
 // (grouped_matmul: block-scaled with per-expert scales; grouped_matmul_swiglu:
 // GEMM + SwiGLU + quantize in one kernel, byte-identical to the chained path).
 //
-// Design (one CTA per SM, persistent):
+// Design (persistent: one CTA per SM, or one CTA pair per two SMs):
 //  * tile scheduler: every CTA builds, in shared memory, the prefix over
-//    groups of ceil(rows_g / 128) * (N / BN) tiles from the device offsets,
-//    then walks tile ids blockIdx.x, blockIdx.x + gridDim.x, ...; a tile id
-//    maps to (group, m-block, n-block) by binary search on that prefix, with
-//    n fastest so that concurrently running CTAs share A rows and B[expert].
+//    groups of ceil(rows_g / (128 * PAIR)) * (N / BN) tiles from the device
+//    offsets, then walks tile ids cid, cid + (number of CTAs or pairs), ...;
+//    a tile id maps to (group, m-block, n-block) by binary search on that
+//    prefix, with n fastest so that concurrently running CTAs share A rows
+//    and B[expert].
+//  * FP4 kinds run M = 256 tiles over a CTA pair (cluster of two,
+//    tcgen05 cta_group::2): each CTA stages its 128 A rows, half of the B
+//    rows and all of the tile's B scales; the even CTA's thread issues the
+//    MMAs for both; FP8 rowwise and MXFP8 run single-CTA 128-row tiles.
 //  * warp 0 (one thread): TMA producer.  A tiles (128 rows x 128 bytes of K)
-//    and B tiles (BN rows x 128 bytes) land 128B-swizzled in a STAGES-deep
-//    shared-memory ring; block-scaled kinds also bulk-copy the 512-byte
-//    scale atoms of the k-tile (contiguous in the tiled scale layout).
+//    and B tiles land 128B-swizzled in a STAGES-deep shared-memory ring;
+//    block-scaled kinds also load the 512-byte scale atoms of the k-tile
+//    (contiguous in the tiled scale layout): tensor copies in pair tiles
+//    (both B row blocks in one 3-D box), 1-D bulk copies otherwise.
 //  * warp 1 (one thread): tcgen05.mma issuer.  The MMAs accumulate in TMEM
 //    (FP8: two 128x256 accumulators, so the epilogue of tile i overlaps the
-//    mainloop of tile i+1; block-scaled: one 128x256 accumulator, because
-//    the per-stage scale slots take the rest of TMEM); tcgen05.commit frees
+//    mainloop of tile i+1; block-scaled: one accumulator, because the
+//    per-stage scale slots take the rest of TMEM); tcgen05.commit frees
 //    ring stages and publishes finished accumulators.
-//  * block-scaled kinds: warp 2 (one thread) moves each stage's scale atoms
-//    shared -> TMEM with tcgen05.cp into that stage's TMEM slot and signals
-//    the MMA thread through a per-stage barrier, so the MMA thread issues
-//    only MMAs.
+//  * block-scaled kinds: two warps (one thread each) move each stage's
+//    scale atoms shared -> TMEM with tcgen05.cp into that stage's TMEM slot
+//    (the atoms dealt alternately) and signal the MMA thread through a
+//    per-stage barrier, so the MMA thread issues only MMAs.
 //  * remaining warps: epilogue.  Each warp owns a 32-lane quarter of TMEM
 //    (one row per thread) and a column range; it reads 32 fp32 columns per
 //    tcgen05.ld, frees the accumulator as soon as its columns are in
-//    registers (single-accumulator kinds), then applies the scales (and
-//    SwiGLU + NVFP4 requant) in registers.
-//  * optional (compile-time, off by default): clusters of two CTAs on
-//    consecutive m-blocks of one expert, each loading half of every B tile
-//    and multicasting it to both.
+//    registers (single-accumulator kinds; in a pair with a relaxed arrive on
+//    the even CTA's barrier), then applies the scales (and SwiGLU + the
+//    requantization) in registers.
 //  * every wait is bounded (about one second) and sets the device error
 //    word instead of hanging.
 #include <cstring>
