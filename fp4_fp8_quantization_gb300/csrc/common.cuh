@@ -18,6 +18,20 @@ __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit) {
     if (err) atomicOr(err, bit);
 }
 
+// Store guard.  Debug builds (MOEQ_DEBUG_BOUNDS) check every global store of
+// the kernels against its buffer's extent first: a store outside it is
+// skipped and sets MOEQ_DEVERR_BOUNDS.  Release builds compile the check out.
+__device__ __forceinline__ bool store_ok(bool in_bounds, uint32_t *err) {
+#ifdef MOEQ_DEBUG_BOUNDS
+    if (!in_bounds) set_error(err, MOEQ_DEVERR_BOUNDS);
+    return in_bounds;
+#else
+    (void)in_bounds;
+    (void)err;
+    return true;
+#endif
+}
+
 // ------------------------------------------------------------------ codecs
 
 // bf16 bits -> fp32 (exact).

@@ -221,7 +221,8 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
                     }
                     w[i] = f32_to_bf16_bits(v0) | (f32_to_bf16_bits(v1) << 16);
                 }
-                st_global_v4(p.c + row * p.N + n, w[0], w[1], w[2], w[3]);
+                if (store_ok(row < p.total_rows && n + 8 <= p.N, p.err))
+                    st_global_v4(p.c + row * p.N + n, w[0], w[1], w[2], w[3]);
             }
         }
         return 0u;
@@ -252,7 +253,7 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
         }
         const uint32_t c0 = nvfp4_codes8(lo8, s.r);
         const uint32_t c1 = nvfp4_codes8(hi8, s.r);
-        if (valid)
+        if (valid && store_ok(row < p.total_rows && nc / 4 + 8 <= p.N / 4, p.err))
             *reinterpret_cast<uint2 *>(p.c_packed + row * (p.N / 4) + nc / 4) = make_uint2(c0, c1);
         return s.code;
     }
@@ -264,6 +265,7 @@ __device__ __forceinline__ void store_sf_bytes(const Params &p, int64_t prow, in
                                                uint32_t bytes, int nblk) {
     const int64_t kv_atoms = p.N / 128;
     const int blk = nc0 / 32;  // first NVFP4 block of the output row
+    if (!store_ok(prow < p.scale_rows_total && blk + nblk <= p.N / 32, p.err)) return;
     uint8_t *w = p.c_sf + sf_word_offset(prow, blk / 4, kv_atoms) + (blk & 3);
     if (nblk == 4)
         *reinterpret_cast<uint32_t *>(w) = bytes;
@@ -348,8 +350,10 @@ __device__ __forceinline__ uint32_t epilogue_mx_block(const Params &p, const uin
                                  : (e4m3x2(h[4 * j], h[4 * j + 1]) |
                                     (e4m3x2(h[4 * j + 2], h[4 * j + 3]) << 16));
             uint8_t *o = p.c_packed + row * (p.N / 2) + nc / 2;
-            st_global_v4(o, w[0], w[1], w[2], w[3]);
-            st_global_v4(o + 16, w[4], w[5], w[6], w[7]);
+            if (store_ok(row < p.total_rows && nc / 2 + 32 <= p.N / 2, p.err)) {
+                st_global_v4(o, w[0], w[1], w[2], w[3]);
+                st_global_v4(o + 16, w[4], w[5], w[6], w[7]);
+            }
         } else {
             uint32_t w[4];
 #pragma unroll
@@ -359,7 +363,8 @@ __device__ __forceinline__ uint32_t epilogue_mx_block(const Params &p, const uin
                 for (int i = 0; i < 8; ++i) x8[i] = h[8 * j + i];
                 w[j] = m == 0.0f ? 0u : e2m1x8(x8);
             }
-            st_global_v4(p.c_packed + row * (p.N / 4) + nc / 4, w[0], w[1], w[2], w[3]);
+            if (store_ok(row < p.total_rows && nc / 4 + 16 <= p.N / 4, p.err))
+                st_global_v4(p.c_packed + row * (p.N / 4) + nc / 4, w[0], w[1], w[2], w[3]);
         }
     }
     return code;
@@ -371,7 +376,8 @@ __device__ __forceinline__ void store_sf_byte_mx(const Params &p, int64_t prow, 
                                                  uint32_t code) {
     const int64_t kv_atoms = (p.N / 64 + 3) / 4;
     const int blk = nc / 64;
-    p.c_sf[sf_word_offset(prow, blk / 4, kv_atoms) + (blk & 3)] = (uint8_t)code;
+    if (store_ok(prow < p.scale_rows_total && blk < p.N / 64, p.err))
+        p.c_sf[sf_word_offset(prow, blk / 4, kv_atoms) + (blk & 3)] = (uint8_t)code;
 }
 
 template <class C, int KIND, int EPI>

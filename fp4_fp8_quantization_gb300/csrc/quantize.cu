@@ -279,13 +279,15 @@ __global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(co
         const int e = gv.eid[gi];
         const uint32_t m = row_abs_max(src, K, lane, v);
         if (e != cur_e) {
-            if (cur_e >= 0 && lane == 0 && cur_m) atomicMax(amax_bits + cur_e, cur_m << 16);
+            if (cur_e >= 0 && lane == 0 && cur_m && store_ok(cur_e < g.num_experts, err))
+                atomicMax(amax_bits + cur_e, cur_m << 16);
             cur_e = e;
             cur_m = 0;
         }
         cur_m = max(cur_m, m);
     }
-    if (cur_e >= 0 && lane == 0 && cur_m) atomicMax(amax_bits + cur_e, cur_m << 16);
+    if (cur_e >= 0 && lane == 0 && cur_m && store_ok(cur_e < g.num_experts, err))
+        atomicMax(amax_bits + cur_e, cur_m << 16);
 }
 
 // amax (fp32 bits of a bf16 value) -> s = amax / 2688, or 1 for amax == 0.
@@ -421,10 +423,12 @@ __global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB) quantize_kernel(Qua
     const uint32_t rg = gv.ro[gi + 1] - r0;
     const uint32_t local = (uint32_t)prow - gv.so[gi];
     if (local >= rg) {  // padding row of this group (up to the next multiple of 128)
-        if (local < ((rg + 127u) & ~127u)) zero_scale_row(p.scales, prow, kv_atoms, lane);
+        if (local < ((rg + 127u) & ~127u) && store_ok(prow < p.g.scale_rows_total, p.err))
+            zero_scale_row(p.scales, prow, kv_atoms, lane);
         return;
     }
     const int64_t row = (int64_t)r0 + local;
+    if (!store_ok(row < p.g.total_rows && prow < p.g.scale_rows_total, p.err)) return;
     const int64_t srow = source_row(p.gt, row, p.err);  // gathered input row
     if (srow < 0) return;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + srow * p.stride);
@@ -531,10 +535,12 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_ker
     const uint32_t rg = gv.ro[gi + 1] - r0;
     const uint32_t local = (uint32_t)prow - gv.so[gi];
     if (local >= rg) {
-        if (local < ((rg + 127u) & ~127u)) zero_scale_row(p.scales, prow, kv_atoms, lane);
+        if (local < ((rg + 127u) & ~127u) && store_ok(prow < p.g.scale_rows_total, p.err))
+            zero_scale_row(p.scales, prow, kv_atoms, lane);
         return;
     }
     const int64_t row = (int64_t)r0 + local;
+    if (!store_ok(row < p.g.total_rows && prow < p.g.scale_rows_total, p.err)) return;
     const float inv = OUT == 0 ? __fdiv_rn(1.0f, gv.scale(gi)) : 0.0f;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;

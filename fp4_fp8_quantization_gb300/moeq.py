@@ -23,6 +23,7 @@ FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp8": 2}
 STATUS = {0: "MOEQ_OK", 1: "MOEQ_ERR_INVALID_ARG", 2: "MOEQ_ERR_UNSUPPORTED",
           3: "MOEQ_ERR_CUDA", 4: "MOEQ_ERR_DEVICE"}
 DEVERR_BAD_OFFSETS, DEVERR_BAD_EXPERT, DEVERR_SCALE_ROWS, DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 1, 2, 4, 8, 16
+DEVERR_BOUNDS = 32   # debug builds only: a store outside its buffer was skipped
 
 _P, _I64, _I32, _U32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32)
 _SIGNATURES = {

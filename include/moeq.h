@@ -77,6 +77,7 @@ typedef enum { MOEQ_NVFP4 = 0, MOEQ_MXFP4 = 1, MOEQ_MXFP8 = 2 } moeq_format;
 #define MOEQ_DEVERR_SCALE_ROWS 0x4u  /* scale offsets unaligned / too small  */
 #define MOEQ_DEVERR_TIMEOUT 0x8u     /* a pipeline wait gave up (~1 s)       */
 #define MOEQ_DEVERR_BAD_INDEX 0x10u  /* gather index outside the input rows  */
+#define MOEQ_DEVERR_BOUNDS 0x20u     /* debug builds: a store outside its buffer was skipped */
 
 /* Per-expert NVFP4 tensor scale of the activations
  * ("grouped_quantize_dynamic_scaled_fp4_async_kernel": sf_tensor, the
