@@ -12,12 +12,14 @@ define them, and the GEMMs dequantize to float64 and use a float64 matmul
 per expert group.  Module map:
 
 * ``formats``  - E2M1 / E4M3 / E8M0 / bf16 encode-decode, nibble packing.
-* ``layout``   - the tiled 128x4 block-scale layout (index function).
+* ``layout``   - the tiled 128x4 block-scale layout (index function) and the
+                 gate/up row interleave of the fused kernel's weight.
 * ``quantize`` - per-expert amax and tensor scale, NVFP4 / MXFP8 / MXFP4
                  block quantization, the grouped (ragged, padded) quantizer.
 * ``gemm``     - grouped rowwise-scaled FP8 GEMM, grouped block-scaled GEMM.
-* ``swiglu``   - the project's exp/SiLU definition and the chained
-                 SwiGLU + NVFP4 requantization.
+* ``swiglu``   - the project's exp / reciprocal / SiLU definition (with an
+                 exact fp32 fused multiply-add emulation) and the chained
+                 SwiGLU + NVFP4 / MX requantization.
 
 Pages cited: "grouped_quantize_dynamic_scaled_fp4_async_kernel" (Mojo kernel
 doc), "grouped_matmul_rowwise_dynamic_scaled_fp8" (Mojo function doc),
