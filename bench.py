@@ -197,7 +197,7 @@ def up_projection_step(d, events=None):
     rec(3)
 
 
-KERNELS_PER_STEP = 5   # padded offsets, amax, amax finalize, quantize, fused GEMM
+KERNELS_PER_STEP = 6   # padded offsets, amax zeroing, amax, amax finalize, quantize, fused GEMM
 
 
 def flops_up(d):

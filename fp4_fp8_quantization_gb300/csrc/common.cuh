@@ -32,6 +32,52 @@ __device__ __forceinline__ bool store_ok(bool in_bounds, uint32_t *err) {
 #endif
 }
 
+// ------------------------------------------------- programmatic launches
+
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl below): its CTAs may be scheduled while the
+// kernel before it in the stream is still finishing.  Each kernel therefore
+// executes pdl_wait() in every thread before its first global memory access
+// (read or write) -- the wait returns once the preceding grid has completed
+// and its memory operations are visible, so the stream order of all memory
+// effects is unchanged -- and pdl_trigger() once its own CTA no longer needs
+// the SM to itself, which lets the next kernel's CTAs launch as this
+// kernel's CTAs drain.  In a kernel launched without the attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Compile-time switch: MOEQ_NO_PDL launches every kernel in plain stream
+// order (the waits and triggers then do nothing).
+#ifdef MOEQ_NO_PDL
+constexpr int kPdl = 0;
+#else
+constexpr int kPdl = 1;
+#endif
+
+// Launches kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialisation; returns the launch status.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = kPdl;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ------------------------------------------------------------------ codecs
 
 // bf16 bits -> fp32 (exact).

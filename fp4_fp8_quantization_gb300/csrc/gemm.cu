@@ -435,6 +435,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             prefetch_tensormap(&tmSFB);
         }
     }
+    // everything above touches only shared memory and the kernel parameters;
+    // from here on global memory written by the preceding kernel is read
+    pdl_wait();
     if (warp == 1) {  // in a pair, warp 1 of both CTAs allocates collectively
         tmem_alloc<C::PAIR>(&tmem_slot, C::TMEM_COLS);
         tmem_relinquish<C::PAIR>();
@@ -780,6 +783,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     }
 
+    // this CTA's loads, MMAs and stores are all issued: the next kernel's
+    // CTAs may launch (they wait for this grid's completion before touching
+    // memory)
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     // neither CTA of a pair leaves while the other may still target it
@@ -940,16 +947,17 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     }
     if (PAIR == 1) {
         const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
-        kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB, tSFA, tSFB, p);
-        return cudaGetLastError();
+        return launch_pdl(kern, grid, C::THREADS, C::SMEM_BYTES, s, tA, tB, tSFA, tSFB, p);
     }
     // persistent CTA pairs (clusters of two): as many as can be resident
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = PAIR;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = kPdl;
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
@@ -965,6 +973,7 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     }
     int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * PAIR), 1, 1);
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSFA, tSFB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

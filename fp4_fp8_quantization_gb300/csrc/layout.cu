@@ -22,6 +22,8 @@ __device__ __forceinline__ int64_t tiled_offset(int64_t r, int64_t c, int64_t kv
 // One thread per byte of the tiled output (padding bytes written as 0).
 __global__ void sf_swizzle_kernel(uint8_t *__restrict__ tiled, const uint8_t *__restrict__ logical,
                                   int64_t batch, int64_t rows, int64_t kv) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t kv_atoms = (kv + 3) / 4;
     const int64_t per_item = (rows + 127) / 128 * kv_atoms * 512;
     const int64_t total = batch * per_item;
@@ -40,6 +42,8 @@ __global__ void sf_swizzle_kernel(uint8_t *__restrict__ tiled, const uint8_t *__
 __global__ void sf_unswizzle_kernel(uint8_t *__restrict__ logical,
                                     const uint8_t *__restrict__ tiled, int64_t batch,
                                     int64_t rows, int64_t kv) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t kv_atoms = (kv + 3) / 4;
     const int64_t per_item = (rows + 127) / 128 * kv_atoms * 512;
     const int64_t total = batch * rows * kv;
@@ -57,6 +61,8 @@ template <typename T>
 __global__ void interleave_rows_kernel(T *__restrict__ out, const T *__restrict__ gate,
                                        const T *__restrict__ up, int64_t batch, int64_t rows,
                                        int64_t words) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t total = batch * rows * 2 * words;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -93,16 +99,15 @@ cudaError_t launch_sf_swizzle(uint8_t *tiled, const uint8_t *logical, int64_t ba
                               int64_t kv, cudaStream_t s) {
     const int64_t n = batch * ((rows + 127) / 128) * ((kv + 3) / 4) * 512;
     if (n == 0) return cudaSuccess;
-    sf_swizzle_kernel<<<grid_for(n), 256, 0, s>>>(tiled, logical, batch, rows, kv);
-    return cudaGetLastError();
+    return launch_pdl(sf_swizzle_kernel, grid_for(n), 256, 0, s, tiled, logical, batch, rows, kv);
 }
 
 cudaError_t launch_sf_unswizzle(uint8_t *logical, const uint8_t *tiled, int64_t batch,
                                 int64_t rows, int64_t kv, cudaStream_t s) {
     const int64_t n = batch * rows * kv;
     if (n == 0) return cudaSuccess;
-    sf_unswizzle_kernel<<<grid_for(n), 256, 0, s>>>(logical, tiled, batch, rows, kv);
-    return cudaGetLastError();
+    return launch_pdl(sf_unswizzle_kernel, grid_for(n), 256, 0, s, logical, tiled, batch, rows,
+                      kv);
 }
 
 cudaError_t launch_interleave_rows(uint8_t *out, const uint8_t *gate, const uint8_t *up,
@@ -111,16 +116,12 @@ cudaError_t launch_interleave_rows(uint8_t *out, const uint8_t *gate, const uint
     const int64_t n = batch * rows * 2 * row_bytes;
     if (n == 0) return cudaSuccess;
     const bool vec = row_bytes % 16 == 0 && ((uintptr_t)out | (uintptr_t)gate | (uintptr_t)up) % 16 == 0;
-    if (vec) {
-        const int64_t words = row_bytes / 16;
-        interleave_rows_kernel<uint4><<<grid_for(n / 16), 256, 0, s>>>(
-            reinterpret_cast<uint4 *>(out), reinterpret_cast<const uint4 *>(gate),
-            reinterpret_cast<const uint4 *>(up), batch, rows, words);
-    } else {
-        interleave_rows_kernel<uint8_t><<<grid_for(n), 256, 0, s>>>(out, gate, up, batch, rows,
-                                                                     row_bytes);
-    }
-    return cudaGetLastError();
+    if (vec)
+        return launch_pdl(interleave_rows_kernel<uint4>, grid_for(n / 16), 256, 0, s,
+                          reinterpret_cast<uint4 *>(out), reinterpret_cast<const uint4 *>(gate),
+                          reinterpret_cast<const uint4 *>(up), batch, rows, row_bytes / 16);
+    return launch_pdl(interleave_rows_kernel<uint8_t>, grid_for(n), 256, 0, s, out, gate, up,
+                      batch, rows, row_bytes);
 }
 
 }  // namespace moeq

@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(co
                                                    Gather gt,
                                                    uint32_t *__restrict__ amax_bits,
                                                    uint32_t *err, int rows_per_warp) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ GroupTable table;
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -290,8 +292,18 @@ __global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(co
         atomicMax(amax_bits + cur_e, cur_m << 16);
 }
 
+// Zeroes the per-expert amax words before amax_kernel's atomics.
+__global__ void zero_words_kernel(uint32_t *buf, int n) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) buf[i] = 0u;
+}
+
 // amax (fp32 bits of a bf16 value) -> s = amax / 2688, or 1 for amax == 0.
 __global__ void amax_finalize_kernel(uint32_t *buf, int E) {
+    pdl_wait();
+    pdl_trigger();
     int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     float amax = __uint_as_float(buf[e]);
@@ -408,6 +420,8 @@ __device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
 // block, or half of an MX block (lanes 2j, 2j+1 share block j).
 template <int FMT, bool A32>
 __global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB) quantize_kernel(QuantParams p) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float r_table[kQWarps][128];
     __shared__ GroupTable table;
     const GroupView gv = load_groups(p.g, FMT == 0 ? p.tensor_scale : nullptr, table);
@@ -523,6 +537,8 @@ struct SwigluParams {
 // 2i+1), 1 MXFP4 / 2 MXFP8 (a 32-h block by lanes 4i .. 4i+3).
 template <int OUT>
 __global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_kernel(SwigluParams p) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ GroupTable table;
     const GroupView gv = load_groups(p.g, OUT == 0 ? p.out_tensor_scale : nullptr, table);
     const int lane = threadIdx.x & 31;
@@ -631,6 +647,8 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_ker
 // ------------------------------------------------------ padded offsets
 
 __global__ void padded_offsets_kernel(const uint32_t *ro, uint32_t *so, int G) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x;
     uint32_t carry = 0;
     if (lane == 0) so[0] = 0;
@@ -658,20 +676,21 @@ __global__ void padded_offsets_kernel(const uint32_t *ro, uint32_t *so, int G) {
 cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const GroupArgs &g,
                               const Gather &gt, float *tensor_scale_out, uint32_t *err,
                               cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(tensor_scale_out, 0, sizeof(float) * g.num_experts, s);
+    uint32_t *bits = reinterpret_cast<uint32_t *>(tensor_scale_out);
+    const unsigned eblocks = (unsigned)((g.num_experts + 255) / 256);
+    cudaError_t e = launch_pdl(zero_words_kernel, eblocks, 256, 0, s, bits, (int)g.num_experts);
     if (e != cudaSuccess) return e;
     if (g.total_rows > 0) {
         // enough warps to fill the GPU on small inputs, 4 rows each on large
         const int rows_per_warp = g.total_rows >= 65536 ? MOEQ_A_RPW : 1;
         int64_t warps = (g.total_rows + rows_per_warp - 1) / rows_per_warp;
         int64_t blocks = (warps + MOEQ_A_WARPS - 1) / MOEQ_A_WARPS;
-        amax_kernel<<<(unsigned)blocks, MOEQ_A_WARPS * 32, 0, s>>>(
-            reinterpret_cast<const uint16_t *>(in), stride, K, g, gt,
-            reinterpret_cast<uint32_t *>(tensor_scale_out), err, rows_per_warp);
+        e = launch_pdl(amax_kernel, (unsigned)blocks, MOEQ_A_WARPS * 32, 0, s,
+                       reinterpret_cast<const uint16_t *>(in), stride, K, g, gt, bits, err,
+                       rows_per_warp);
+        if (e != cudaSuccess) return e;
     }
-    amax_finalize_kernel<<<(g.num_experts + 255) / 256, 256, 0, s>>>(
-        reinterpret_cast<uint32_t *>(tensor_scale_out), g.num_experts);
-    return cudaGetLastError();
+    return launch_pdl(amax_finalize_kernel, eblocks, 256, 0, s, bits, (int)g.num_experts);
 }
 
 cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,
@@ -683,22 +702,17 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
     if (blocks == 0) return cudaSuccess;
     // 256-bit loads need every row start 32-byte aligned
     const bool a32 = (reinterpret_cast<uintptr_t>(in) % 32 == 0) && (stride % 16 == 0);
-    if (fmt == 0)
-        a32 ? quantize_kernel<0, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
-            : quantize_kernel<0, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
-    else if (fmt == 1)
-        a32 ? quantize_kernel<1, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
-            : quantize_kernel<1, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
-    else
-        a32 ? quantize_kernel<2, true><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p)
-            : quantize_kernel<2, false><<<(unsigned)blocks, kQWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    void (*kern)(QuantParams) =
+        fmt == 0 ? (a32 ? quantize_kernel<0, true> : quantize_kernel<0, false>)
+        : fmt == 1 ? (a32 ? quantize_kernel<1, true> : quantize_kernel<1, false>)
+                   : (a32 ? quantize_kernel<2, true> : quantize_kernel<2, false>);
+    return launch_pdl(kern, (unsigned)blocks, kQWarps * 32, 0, s, p);
 }
 
 cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_offsets,
                                   int32_t num_groups, cudaStream_t s) {
-    padded_offsets_kernel<<<1, 32, 0, s>>>(row_offsets, scales_offsets, num_groups);
-    return cudaGetLastError();
+    return launch_pdl(padded_offsets_kernel, 1, 32, 0, s, row_offsets, scales_offsets,
+                      (int)num_groups);
 }
 
 cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, const void *y,
@@ -707,13 +721,10 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
     SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
     int64_t blocks = (g.scale_rows_total + kSWarps - 1) / kSWarps;
     if (blocks == 0) return cudaSuccess;
-    if (out_fmt == 0)
-        swiglu_quantize_kernel<0><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
-    else if (out_fmt == 1)
-        swiglu_quantize_kernel<1><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
-    else
-        swiglu_quantize_kernel<2><<<(unsigned)blocks, kSWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    void (*kern)(SwigluParams) = out_fmt == 0   ? swiglu_quantize_kernel<0>
+                                 : out_fmt == 1 ? swiglu_quantize_kernel<1>
+                                                : swiglu_quantize_kernel<2>;
+    return launch_pdl(kern, (unsigned)blocks, kSWarps * 32, 0, s, p);
 }
 
 }  // namespace moeq
