@@ -56,7 +56,8 @@ def parse_args():
     p.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     p.add_argument("--no-parts", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained"],
+    p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained",
+                                          "swiglu"],
                    help="run only --warmup + --steps launches of one kernel on a small case "
                         "(inputs larger than L2, under 1 GB) for a profiler; no JSON line")
     return p.parse_args()
@@ -666,7 +667,7 @@ def run_profile_case(args):
     from fp4_fp8_quantization_gb300 import moeq, synth
     dev = "cuda"
     u32 = lambda a: torch.from_numpy(np.asarray(a, np.uint32).view(np.int32)).to(dev)
-    if args.profile in ("fused", "chained", "quantize"):
+    if args.profile in ("fused", "chained", "quantize", "swiglu"):
         # 32 experts, 4096 tokens top-8 -> 32768 rows, K 4096, I 1536
         counts = synth.routing_counts(4096, 8, 32, seed=0)
         ro, ids = synth.ragged_groups(counts)
@@ -701,6 +702,10 @@ def run_profile_case(args):
             if args.profile == "fused":
                 fn = lambda: moeq.grouped_matmul_swiglu(c, csf, a, asf, b, bsf, es, ots, ro_d,
                                                         so_d, ids_d, I4, K4, rows)
+            elif args.profile == "swiglu":
+                # the chained SwiGLU + NVFP4 requant on a 201 MB bf16 gate/up matrix
+                y = synth.bf16_normal((T, N), 1.0, seed=7, device=dev)
+                fn = lambda: moeq.swiglu_quantize(c, csf, y, ots, ro_d, so_d, ids_d, 32, rows)
             else:
                 y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
                 fn = lambda: moeq.grouped_matmul_blockscaled("nvfp4", y, a, asf, b, bsf, es, ro_d,
