@@ -48,6 +48,15 @@ FP8_OVER_BF16 = 4.5 / 2.25
 FUSED_TRAFFIC_BYTES = 1.3218e9
 
 
+def emit(line, args):
+    """Prints the result line; appends it to the metrics log when one is named."""
+    text = json.dumps(line)
+    print(text, flush=True)
+    if args.log:
+        with open(args.log, "a") as f:
+            f.write(text + "\n")
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -56,6 +65,8 @@ def parse_args():
     p.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     p.add_argument("--no-parts", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--log", default=os.environ.get("MOEQ_METRICS_LOG"),
+                   help="also append the JSON line to this file (default: $MOEQ_METRICS_LOG)")
     p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained",
                                           "swiglu"],
                    help="run only --warmup + --steps launches of one kernel on a small case "
@@ -499,7 +510,7 @@ def run_reference(args, rank, world):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    emit(line, args)
 
 
 def run_moeq(args, rank, world):
@@ -658,7 +669,7 @@ def run_moeq(args, rank, world):
             "clocks": clk, "roofline": roof, "breakdown": breakdown, "e2e": e2e,
             "cpu_baseline": cpu, "parts": extra, "device_error": err,
         }
-        print(json.dumps(line), flush=True)
+        emit(line, args)
 
 
 def run_profile_case(args):

@@ -47,6 +47,16 @@ def bf16_values(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+# Fields of the running test's metrics line (written by conftest.py when
+# MOEQ_METRICS_LOG names a file).
+NOTES = {}
+
+
+def note(**fields):
+    """Adds fields (sizes, error figures) to the running test's metrics line."""
+    NOTES.update(fields)
+
+
 def assert_gemm_close(gpu_bits, ref_f64, mask_rows=None):
     """Per element |gpu - ref| <= max(2 ulp_bf16(ref), 1e-3 * rms(ref)),
     ulp_bf16(x) = 2^(floor(log2|x|) - 7), rms over the compared elements."""
@@ -61,6 +71,12 @@ def assert_gemm_close(gpu_bits, ref_f64, mask_rows=None):
     tol = np.maximum(2 * ulp, 1e-3 * rms)
     err = np.abs(got - ref)
     bad = err > tol
+    if err.size:
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(err == 0, 0.0, err / tol)   # inf where tol is 0 and err is not
+        note(compared=NOTES.get("compared", 0) + int(err.size),
+             max_abs_err=max(NOTES.get("max_abs_err", 0.0), float(err.max())),
+             max_err_over_tol=max(NOTES.get("max_err_over_tol", 0.0), float(ratio.max())))
     assert not bad.any(), (
         f"{bad.sum()} of {bad.size} outside tolerance; worst err {err.max():.4g} "
         f"(tol there {tol.reshape(-1)[np.argmax(err)]:.4g}), rms {rms:.4g}")
