@@ -20,10 +20,14 @@ per expert group.  Module map:
 * ``swiglu``   - the project's exp / reciprocal / SiLU definition (with an
                  exact fp32 fused multiply-add emulation) and the chained
                  SwiGLU + NVFP4 / MX requantization.
+* ``dispatch`` - the single-rank expert dispatch: routing of top-k choices
+                 to expert groups and MXFP4 quantization of the routed rows
+                 (padded or fixed-slot scale layout).
 
 Pages cited: "grouped_quantize_dynamic_scaled_fp4_async_kernel" (Mojo kernel
 doc), "grouped_matmul_rowwise_dynamic_scaled_fp8" (Mojo function doc),
-"max.nn.moe.NvMxf4f8Strategy" (Python class doc).
+"max.nn.moe.NvMxf4f8Strategy" (Python class doc), "Struct_ep_dispatch_mxfp4"
+(Mojo graph-op doc).
 
 Parity unpinned: behaviour on NaN / Inf inputs (the synthetic data holds
 none and the library leaves it undefined).
