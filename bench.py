@@ -351,6 +351,30 @@ def parts(pk, flush):
         "ms": round(ms, 4), "GB/s_active_weights": round(wbytes / ms / 1e6, 1),
         "frac_hbm": round(wbytes / ms / 1e6 / hbm, 4)}
     del a, b8, c
+    # single-rank expert dispatch: 16384 tokens routed top-8 over 128
+    # experts, hidden 4096 -> 131072 MXFP4 rows (routing + gather-quantize)
+    tok = synth.bf16_normal((TOK4, K4), 1.0, seed=70, device=dev)
+    tk = torch.from_numpy(synth.topk_ids(TOK4, TOPK4, E4, seed=0)).to(dev)
+    n_rows = TOK4 * TOPK4
+    rows_d = moeq.dispatch_scale_rows(TOK4, TOPK4, E4)
+    q_d = torch.empty((n_rows, K4 // 2), dtype=torch.uint8, device=dev)
+    sf_d = torch.empty(moeq.sf_bytes(rows_d, K4 // 32), dtype=torch.uint8, device=dev)
+    ro_dd = torch.empty(E4 + 1, dtype=torch.int32, device=dev)
+    eid_d = torch.empty(E4, dtype=torch.int32, device=dev)
+    src_d = torch.empty(n_rows, dtype=torch.int32, device=dev)
+    so_dd = torch.empty(E4 + 1, dtype=torch.int32, device=dev)
+    t_route = time_kernel(lambda: moeq.route_topk(tk, ro_dd, eid_d, src_d, so_dd), 20, batch=8)
+    t_disp = time_kernel(lambda: moeq.dispatch_mxfp4(tok, tk, q_d, sf_d, ro_dd, eid_d, src_d,
+                                                     so_dd), 10)
+    used_sf = int(so_dd[-1].item()) // 128 * (K4 // 32 // 4) * 512
+    nbytes = tok.numel() * 2 + q_d.numel() + used_sf + tk.numel() * 4
+    out["dispatch_mxfp4_16384tok_top8_128experts"] = {
+        "route_us": round(t_route * 1e3, 2), "ms": round(t_disp, 4),
+        "GB/s": round(nbytes / t_disp / 1e6, 1), "bytes": nbytes,
+        "bytes_note": "tokens read once + MXFP4 rows + used scale rows + top-k ids; the "
+                      "gather reads every token top_k times (1.07 GB of row reads)",
+        "timing": "route: median of 20 batches of 8 calls; dispatch: mean of 10 calls"}
+    del tok
     return out
 
 

@@ -239,6 +239,76 @@ moeq_status moeq_grouped_quantize_gather(moeq_format fmt, const void *in, int64_
                          num_active_experts, gt, stream);
 }
 
+// ------------------------------------------------------------ dispatch
+
+static moeq_status route_args_ok(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
+                                 int32_t num_experts, const uint32_t *row_offsets,
+                                 const int32_t *expert_ids, const int32_t *src_info,
+                                 const uint32_t *scales_offsets, int32_t slot_rows) {
+    if (num_tokens < 0 || top_k < 1 || num_experts < 1 || slot_rows < 0 || slot_rows % 128)
+        return MOEQ_ERR_INVALID_ARG;
+    if (num_experts > moeq::kRouteMaxExperts || num_tokens >= ((int64_t)1 << 31) / top_k)
+        return MOEQ_ERR_UNSUPPORTED;
+    if (!row_offsets || !expert_ids || !aligned16(row_offsets) || !aligned16(expert_ids))
+        return MOEQ_ERR_INVALID_ARG;
+    if (scales_offsets && !aligned16(scales_offsets)) return MOEQ_ERR_INVALID_ARG;
+    if (num_tokens > 0 &&
+        (!topk_ids || !src_info || !aligned16(topk_ids) || !aligned16(src_info)))
+        return MOEQ_ERR_INVALID_ARG;
+    return MOEQ_OK;
+}
+
+moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
+                            int32_t num_experts, uint32_t *row_offsets, int32_t *expert_ids,
+                            int32_t *src_info, uint32_t *scales_offsets, int32_t slot_rows,
+                            moeq_stream_t stream) {
+    const moeq_status st = route_args_ok(topk_ids, num_tokens, top_k, num_experts, row_offsets,
+                                         expert_ids, src_info, scales_offsets, slot_rows);
+    if (st != MOEQ_OK) return st;
+    uint32_t *err = device_error_ptr();
+    if (!err) return cuda_status(cudaErrorInvalidDevice);
+    return cuda_status(moeq::launch_route_topk(topk_ids, num_tokens * top_k, num_experts,
+                                               row_offsets, expert_ids, src_info, scales_offsets,
+                                               slot_rows, err, stream));
+}
+
+int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_experts,
+                                 int32_t slot_rows) {
+    if (num_tokens < 0 || top_k < 1 || num_experts < 1 || slot_rows < 0 ||
+        num_tokens >= ((int64_t)1 << 31) / top_k)
+        return -1;
+    if (slot_rows > 0) return (int64_t)num_experts * slot_rows;
+    // sum over experts of ceil(r_e / 128) * 128 <= sum (r_e + 127), a multiple of 128
+    return (num_tokens * top_k + 127 * (int64_t)num_experts) / 128 * 128;
+}
+
+moeq_status moeq_dispatch_mxfp4(const void *tokens, int64_t token_stride, int64_t num_tokens,
+                                int64_t hidden, const int32_t *topk_ids, int32_t top_k,
+                                int32_t num_experts, uint8_t *out, uint8_t *scales,
+                                int64_t scale_rows_total, uint32_t *row_offsets,
+                                int32_t *expert_ids, int32_t *src_info,
+                                uint32_t *scales_offsets, int32_t slot_rows,
+                                moeq_stream_t stream) {
+    moeq_status st = route_args_ok(topk_ids, num_tokens, top_k, num_experts, row_offsets,
+                                   expert_ids, src_info, scales_offsets, slot_rows);
+    if (st != MOEQ_OK) return st;
+    // every check of the quantization step before anything is launched
+    if (!scales_offsets || hidden <= 0 || hidden % 128 || token_stride < hidden ||
+        token_stride % 8 || scale_rows_total % 128 ||
+        scale_rows_total < moeq_dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows))
+        return MOEQ_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!tokens || !out || !scales || !aligned16(tokens) || !aligned16(out) ||
+                           !aligned16(scales)))
+        return MOEQ_ERR_INVALID_ARG;
+    st = moeq_route_topk(topk_ids, num_tokens, top_k, num_experts, row_offsets, expert_ids,
+                         src_info, scales_offsets, slot_rows, stream);
+    if (st != MOEQ_OK || num_tokens == 0) return st;
+    const moeq::Gather gt{src_info, top_k, num_tokens};
+    return quantize_impl(MOEQ_MXFP4, tokens, token_stride, num_tokens * top_k, hidden, out,
+                         scales, scale_rows_total, row_offsets, scales_offsets, expert_ids,
+                         nullptr, num_experts, num_experts, gt, stream);
+}
+
 moeq_status moeq_grouped_matmul_rowwise_fp8(void *c, const uint8_t *a, const uint8_t *b,
                                             const float *a_scales, const float *b_scales,
                                             const uint32_t *a_offsets,

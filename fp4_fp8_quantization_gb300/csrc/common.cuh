@@ -460,6 +460,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
     return r;
 }
 
+// 32-bit load from the shared memory of a CTA of the cluster (address from
+// mapa_shared).
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Arrival on a barrier given by its shared::cluster address (possibly in
 // the other CTA of the pair), releasing at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {

@@ -51,6 +51,15 @@ cudaError_t launch_interleave_rows(uint8_t *out, const uint8_t *gate, const uint
                                    int64_t batch, int64_t rows, int64_t row_bytes,
                                    cudaStream_t s);
 
+// Routing of top-k choices to expert groups (route.cu); at most
+// kRouteMaxExperts experts.  slot_rows > 0: scales_offsets[e] = e * slot_rows,
+// else the padded prefix; scales_offsets may be null.
+constexpr int kRouteMaxExperts = 1024;
+cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int num_experts,
+                              uint32_t *row_offsets, int32_t *expert_ids, int32_t *src_info,
+                              uint32_t *scales_offsets, int slot_rows, uint32_t *err,
+                              cudaStream_t s);
+
 // Grouped GEMMs.  kind: 0 = FP8 rowwise, 1 = NVFP4 block-scaled,
 // 2 = MXFP8 block-scaled, 3 = MXFP4 block-scaled.  epi: 0 = bf16 out,
 // 1 = fused SwiGLU + NVFP4, 2 = fused SwiGLU + MX in the mainloop's format.

@@ -49,6 +49,10 @@ _SIGNATURES = {
     "moeq_sf_swizzle": [_P, _P, _I64, _I64, _I64, _P],
     "moeq_sf_unswizzle": [_P, _P, _I64, _I64, _I64, _P],
     "moeq_interleave_gate_up": [_P, _P, _P, _I64, _I64, _I64, _P],
+    "moeq_route_topk": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P],
+    "moeq_dispatch_scale_rows": [_I64, _I32, _I32, _I32],
+    "moeq_dispatch_mxfp4": [_P, _I64, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P,
+                            _I32, _P],
     "moeq_get_device_error": [_P, _U32P],
     "moeq_clear_device_error": [_P],
     "moeq_last_cuda_error": [],
@@ -77,6 +81,7 @@ def lib():
             f.argtypes = args
             f.restype = ctypes.c_int
         L.moeq_status_string.restype = ctypes.c_char_p
+        L.moeq_dispatch_scale_rows.restype = ctypes.c_int64
         _lib = L
     return _lib
 
@@ -207,6 +212,53 @@ def interleave_gate_up(out, gate, up, stream=None):
         raise ValueError("out: expected batch * 2 * rows * row_bytes bytes")
     _call("moeq_interleave_gate_up", _ptr(out, _U8, "out"), _ptr(gate, _U8, "gate"),
           _ptr(up, _U8, "up"), batch, rows, rb, _stream(stream))
+
+
+def route_topk(topk_ids, row_offsets, expert_ids, src_info, scales_offsets=None, slot_rows=0,
+               stream=None):
+    """Routes the choices of topk_ids (int32 [num_tokens, top_k]) to the
+    groups of their experts: row_offsets (int32/uint32 [E + 1]), expert_ids
+    (int32 [E]), src_info (int32 [num_tokens * top_k]) and, if given,
+    scales_offsets ([E + 1]: padded, or slots of slot_rows rows)."""
+    if topk_ids.dim() != 2:
+        raise ValueError("topk_ids: expected [num_tokens, top_k]")
+    E = expert_ids.numel()
+    if row_offsets.numel() != E + 1 or src_info.numel() < topk_ids.numel():
+        raise ValueError("row_offsets [E + 1] and src_info [num_tokens * top_k] expected")
+    _call("moeq_route_topk", _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[0],
+          topk_ids.shape[1], E, _ptr(row_offsets, _U32, "row_offsets"),
+          _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(src_info, torch.int32, "src_info"),
+          _ptr(scales_offsets, _U32, "scales_offsets"), slot_rows, _stream(stream))
+
+
+def dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows=0):
+    """Logical scale rows dispatch_mxfp4 needs for these sizes."""
+    n = lib().moeq_dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows)
+    if n < 0:
+        raise ValueError("invalid sizes")
+    return n
+
+
+def dispatch_mxfp4(tokens, topk_ids, out, scales, row_offsets, expert_ids, src_info,
+                   scales_offsets, slot_rows=0, stream=None):
+    """Single-rank expert dispatch: route_topk, then MXFP4 quantization of
+    the routed rows (row r is token src_info[r] // top_k).  tokens bf16
+    [num_tokens, hidden]; out uint8 [num_tokens * top_k, hidden / 2]; scales
+    the tiled E8M0 buffer (sf_bytes(rows, hidden / 32) bytes for
+    rows = dispatch_scale_rows(...) or more, a multiple of 128)."""
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != tokens.shape[0]:
+        raise ValueError("topk_ids: expected [num_tokens, top_k]")
+    T, H = tokens.shape
+    E = expert_ids.numel()
+    if out.numel() < topk_ids.numel() * (H // 2) or row_offsets.numel() != E + 1:
+        raise ValueError("out [num_tokens * top_k, hidden / 2] and row_offsets [E + 1] expected")
+    rows = scales.numel() // max(1, sf_bytes(128, H // 32)) * 128
+    _call("moeq_dispatch_mxfp4", _ptr_rows(tokens, torch.bfloat16, "tokens"), tokens.stride(0),
+          T, H, _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[1], E,
+          _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"), rows,
+          _ptr(row_offsets, _U32, "row_offsets"), _ptr(expert_ids, torch.int32, "expert_ids"),
+          _ptr(src_info, torch.int32, "src_info"), _ptr(scales_offsets, _U32, "scales_offsets"),
+          slot_rows, _stream(stream))
 
 
 def grouped_matmul_rowwise_fp8(c, a, b, a_scales, b_scales, a_offsets, expert_ids,

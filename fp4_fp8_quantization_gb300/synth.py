@@ -23,16 +23,22 @@ import numpy as np
 import torch
 
 
-def routing_counts(num_tokens, top_k, num_experts, seed=0, zipf_s=None):
-    """Rows per expert when each of ``num_tokens`` tokens is routed to
-    ``top_k`` distinct experts."""
+def topk_ids(num_tokens, top_k, num_experts, seed=0, zipf_s=None):
+    """int32 [num_tokens, top_k]: the ``top_k`` distinct experts each token is
+    routed to (uniform, or weighted by p_e ~ (e + 1)^-zipf_s)."""
     rng = np.random.default_rng(seed)
     if zipf_s is None:
         logp = np.zeros(num_experts)
     else:
         logp = -zipf_s * np.log(np.arange(1, num_experts + 1, dtype=np.float64))
     keys = logp[None, :] + rng.gumbel(size=(num_tokens, num_experts))
-    chosen = np.argpartition(-keys, top_k - 1, axis=1)[:, :top_k]
+    return np.argpartition(-keys, top_k - 1, axis=1)[:, :top_k].astype(np.int32)
+
+
+def routing_counts(num_tokens, top_k, num_experts, seed=0, zipf_s=None):
+    """Rows per expert when each of ``num_tokens`` tokens is routed to
+    ``top_k`` distinct experts (the choices of topk_ids)."""
+    chosen = topk_ids(num_tokens, top_k, num_experts, seed, zipf_s)
     return np.bincount(chosen.reshape(-1), minlength=num_experts).astype(np.int64)
 
 

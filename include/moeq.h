@@ -329,6 +329,63 @@ moeq_status moeq_interleave_gate_up(uint8_t *out, const uint8_t *gate, const uin
                                     int64_t batch, int64_t rows, int64_t row_bytes,
                                     moeq_stream_t stream);
 
+/* Expert dispatch on one rank ("Struct_ep_dispatch_mxfp4", execute: the
+ * row_offsets, expert_ids and src_info outputs and the MXFP4 tokens; with a
+ * single rank the all-to-all exchange is the identity and is not built).
+ *
+ * moeq_route_topk routes every choice i = t * top_k + k of topk_ids to the
+ * group of its expert.  Group e is expert e for all e in [0, num_experts),
+ * empty groups included; a group's rows hold its choices in increasing i
+ * (a stable order: the page's atomic counters leave the order open).
+ *   topk_ids        int32 [num_tokens, top_k] (device), expert of each choice.
+ *   row_offsets     u32 [num_experts + 1] (out)
+ *   expert_ids      int32 [num_experts] (out): 0 .. num_experts - 1
+ *   src_info        int32 [num_tokens * top_k] (out): row r holds choice
+ *                   src_info[r] (token src_info[r] / top_k); entries past
+ *                   row_offsets[num_experts] are not written.
+ *   scales_offsets  u32 [num_experts + 1] (out, may be NULL): with
+ *                   slot_rows == 0 the padded prefix of ceil(r_e / 128) * 128
+ *                   (as moeq_padded_scale_offsets); with slot_rows > 0 (a
+ *                   multiple of 128) the fixed-stride slots e * slot_rows of
+ *                   the page's scale-slot fusion (fuse_a_scale_preshuffle,
+ *                   slot stride max_padded_M).
+ * A choice whose expert id lies outside [0, num_experts) is dropped and sets
+ * MOEQ_DEVERR_BAD_EXPERT.  Limits: 1 <= num_experts <= 1024 (else
+ * MOEQ_ERR_UNSUPPORTED), num_tokens * top_k < 2^31.  One CTA on one SM; no
+ * memory besides the outputs. */
+moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
+                            int32_t num_experts, uint32_t *row_offsets, int32_t *expert_ids,
+                            int32_t *src_info, uint32_t *scales_offsets, int32_t slot_rows,
+                            moeq_stream_t stream);
+
+/* Scale rows that moeq_dispatch_mxfp4 needs: num_experts * slot_rows with
+ * slot_rows > 0, else the largest possible padded total,
+ * floor((num_tokens * top_k + 127 * num_experts) / 128) * 128.  Host only. */
+int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_experts,
+                                 int32_t slot_rows);
+
+/* moeq_route_topk, then MXFP4 quantization of the routed rows (routed row r
+ * is token src_info[r] / top_k; moeq_grouped_quantize_gather with
+ * indices = src_info, indices_divisor = top_k), in stream order.
+ *   tokens          bf16 [num_tokens, hidden], row stride token_stride
+ *                   elements; hidden a multiple of 128.
+ *   out             uint8 [num_tokens * top_k, hidden / 2] packed E2M1
+ *                   (rows past the routed count are not written).
+ *   scales          tiled E8M0 block scales of scale_rows_total logical rows
+ *                   of hidden / 32 scales; scale_rows_total >=
+ *                   moeq_dispatch_scale_rows(...) and a multiple of 128.
+ *   row_offsets, expert_ids, src_info, scales_offsets: as moeq_route_topk
+ *                   (scales_offsets required here).
+ * With slot_rows > 0 a group larger than slot_rows is not quantized and
+ * sets MOEQ_DEVERR_SCALE_ROWS. */
+moeq_status moeq_dispatch_mxfp4(const void *tokens, int64_t token_stride, int64_t num_tokens,
+                                int64_t hidden, const int32_t *topk_ids, int32_t top_k,
+                                int32_t num_experts, uint8_t *out, uint8_t *scales,
+                                int64_t scale_rows_total, uint32_t *row_offsets,
+                                int32_t *expert_ids, int32_t *src_info,
+                                uint32_t *scales_offsets, int32_t slot_rows,
+                                moeq_stream_t stream);
+
 /* Reads the sticky device error word of the current device (MOEQ_DEVERR_*
  * bits) after synchronising `stream`.  Returns MOEQ_ERR_DEVICE when any bit
  * is set, MOEQ_OK otherwise. */

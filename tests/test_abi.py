@@ -82,6 +82,39 @@ def test_layout_helpers_reject_bad_host_arguments(lib):
     assert il(None, None, None, 2, 4, 0, None) == 0
 
 
+def test_route_and_dispatch_reject_bad_host_arguments(lib):
+    r = lib.moeq_route_topk
+    #        ids   T   k  E    ro    eids  src   so    slot stream
+    assert r(FAKE, 8, 0, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # top_k < 1
+    assert r(FAKE, 8, 2, 0, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # no experts
+    assert r(FAKE, 8, 2, 2000, FAKE, FAKE, FAKE, FAKE, 0, None) == 2   # above 1024 experts
+    assert r(FAKE, 8, 2, 4, FAKE, FAKE, FAKE, FAKE, 100, None) == 1    # slot % 128
+    assert r(FAKE, 8, 2, 4, None, FAKE, FAKE, FAKE, 0, None) == 1      # row_offsets
+    assert r(None, 8, 2, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # topk_ids with tokens
+    assert r(FAKE, 8, 2, 4, FAKE, FAKE, ODD, FAKE, 0, None) == 1       # misaligned
+    assert r(FAKE, 1 << 30, 4, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 2   # 2^32 choices
+    rows = lib.moeq_dispatch_scale_rows
+    assert rows(100, 8, 16, 0) == (800 + 127 * 16) // 128 * 128
+    assert rows(100, 8, 16, 256) == 16 * 256
+    assert rows(-1, 8, 16, 0) == -1
+    d = lib.moeq_dispatch_mxfp4
+    ok = dict(tok=FAKE, stride=256, T=8, H=256, ids=FAKE, k=2, E=4, out=FAKE, sf=FAKE,
+              srows=rows(8, 2, 4, 0), ro=FAKE, eids=FAKE, src=FAKE, so=FAKE, slot=0, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return d(a["tok"], a["stride"], a["T"], a["H"], a["ids"], a["k"], a["E"], a["out"],
+                 a["sf"], a["srows"], a["ro"], a["eids"], a["src"], a["so"], a["slot"], a["s"])
+
+    assert call(H=200) == 1                 # hidden % 128
+    assert call(stride=128) == 1            # stride < hidden
+    assert call(srows=0) == 1               # no scale rows
+    assert call(srows=ok["srows"] - 128) == 1   # fewer scale rows than needed
+    assert call(so=None) == 1               # scale offsets required
+    assert call(out=ODD) == 1
+    assert call(slot=128, srows=4 * 128 - 128) == 1
+
+
 def test_gemms_reject_bad_host_arguments(lib):
     r = lib.moeq_grouped_matmul_rowwise_fp8
     #        c     a     b     sa    sb    ao    ids   T   N    K    E  mt  G  stream

@@ -145,3 +145,24 @@ def test_swiglu_and_layout_entry_points_stay_in_their_buffers():
     moeq.interleave_gate_up(out, gate, up)
     g.check()
     assert moeq.get_device_error() == 0
+
+
+def test_dispatch_entry_points_stay_in_their_buffers():
+    need_gpu()
+    moeq.clear_device_error()
+    T, H, E, k = 300, 256, 7, 3
+    g = Guarded()
+    tok = synth.bf16_normal((T, H), 1.0, seed=31, device=DEV)
+    ids = torch.from_numpy(synth.topk_ids(T, k, E, seed=32, zipf_s=1.0)).to(DEV)
+    for slot in (0, 384):
+        ro = g((E + 1,), torch.int32)
+        eids = g((E,), torch.int32)
+        src = g((T * k,), torch.int32)
+        so = g((E + 1,), torch.int32)
+        moeq.route_topk(ids, ro, eids, src, so, slot)
+        rows = moeq.dispatch_scale_rows(T, k, E, slot)
+        out = g((T * k, H // 2), torch.uint8)
+        sf = g((moeq.sf_bytes(rows, H // 32),), torch.uint8)
+        moeq.dispatch_mxfp4(tok, ids, out, sf, ro, eids, src, so, slot)
+    g.check()
+    assert moeq.get_device_error() == 0
