@@ -537,6 +537,142 @@ def run_reference(args, rank, world):
     emit(line, args)
 
 
+def token_step(B, d):
+    """The up-projection from tokens and their top-k ids: routing, per-expert
+    amax and NVFP4 quantization of the gathered rows, fused GEMM + SwiGLU +
+    requant (the same GEMM work as up_projection_step)."""
+    from fp4_fp8_quantization_gb300 import moeq
+    moeq.route_topk(B["tk"], B["ro"], B["ids"], B["src"], B["so"])
+    moeq.grouped_amax_scale_gather(B["tok"], B["src"], TOPK4, B["ro"], B["ids"], B["ts"], E4)
+    moeq.grouped_quantize_gather("nvfp4", B["tok"], B["src"], TOPK4, B["a"], B["asf"], B["ro"],
+                                 B["so"], B["ids"], B["ts"], E4, B["rows"])
+    moeq.grouped_matmul_swiglu(B["c"], B["csf"], B["a"], B["asf"], d["b"], d["bsf"], d["es"],
+                               d["ots"], B["ro"], B["so"], B["ids"], I4, K4, B["rows"])
+
+
+def run_e2e(d, args, world, fl, form):
+    """Pipelined steps from pinned host buffers through the public calls: the
+    host->device copy of step i+1 (split over four copy streams) overlaps the
+    compute of step i, the device->host copy of the packed output and its
+    scales runs on its own stream, two device buffer sets alternate.
+    form "tokens": H2D of the 16384 bf16 tokens + top-8 ids, token_step;
+    form "rows": H2D of the 131072 gathered rows + group offsets,
+    up_projection_step."""
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    n_copy = 4
+    if form == "tokens":
+        host = {"tok": synth.bf16_normal((TOK4, K4), 1.0, seed=80).pin_memory(),
+                "tk": torch.from_numpy(synth.topk_ids(TOK4, TOPK4, E4, seed=0)).pin_memory()}
+        split = "tok"
+        rows = moeq.dispatch_scale_rows(TOK4, TOPK4, E4)
+        n = TOK4 * TOPK4
+
+        def buffers():
+            return {"tok": torch.empty((TOK4, K4), dtype=torch.bfloat16, device="cuda"),
+                    "tk": torch.empty((TOK4, TOPK4), dtype=torch.int32, device="cuda"),
+                    "ro": torch.empty(E4 + 1, dtype=torch.int32, device="cuda"),
+                    "ids": torch.empty(E4, dtype=torch.int32, device="cuda"),
+                    "src": torch.empty(n, dtype=torch.int32, device="cuda"),
+                    "so": torch.empty(E4 + 1, dtype=torch.int32, device="cuda"),
+                    "ts": torch.empty(E4, device="cuda"),
+                    "a": torch.empty((n, K4 // 2), dtype=torch.uint8, device="cuda"),
+                    "asf": torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8,
+                                       device="cuda"),
+                    "c": torch.empty((n, I4 // 2), dtype=torch.uint8, device="cuda"),
+                    "csf": torch.empty(moeq.sf_bytes(rows, I4 // 16), dtype=torch.uint8,
+                                       device="cuda"),
+                    "rows": rows}
+
+        def compute(B):
+            token_step(B, d)
+    else:
+        host = {"x": d["x"].cpu().pin_memory(), "ro": d["ro"].cpu().pin_memory(),
+                "ids": d["ids"].cpu().pin_memory()}
+        split = "x"
+
+        def buffers():
+            B = dict(d)
+            for k in ("x", "ro", "ids", "so", "ts", "a", "asf", "c", "csf"):
+                B[k] = torch.empty_like(d[k])
+            return B
+
+        def compute(B):
+            up_projection_step(B)
+    bufs = [buffers(), buffers()]
+    chs = [torch.empty(bufs[0]["c"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    sfhs = [torch.empty(bufs[0]["csf"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    h2d_streams = [torch.cuda.Stream() for _ in range(n_copy)]
+    d2h_stream = torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    comp_done, d2h_done = [None, None], [None, None]
+    steps = max(3, min(args.steps, 20))
+
+    def issue(i):
+        b = i % 2
+        B = bufs[b]
+        total = host[split].shape[0]
+        chunk = (total + n_copy - 1) // n_copy
+        ready = []
+        for j, st in enumerate(h2d_streams):
+            if comp_done[b] is not None:       # step i-2 has finished reading buffer b
+                st.wait_event(comp_done[b])
+            with torch.cuda.stream(st):
+                r0, r1 = j * chunk, min(total, (j + 1) * chunk)
+                B[split][r0:r1].copy_(host[split][r0:r1], non_blocking=True)
+                if j == 0:
+                    for k, t in host.items():
+                        if k != split:
+                            B[k].copy_(t, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                ready.append(ev)
+        for ev in ready:
+            comp.wait_event(ev)
+        if d2h_done[b] is not None:             # outputs of step i-2 are on the host
+            comp.wait_event(d2h_done[b])
+        compute(B)
+        cd = torch.cuda.Event()
+        cd.record(comp)
+        comp_done[b] = cd
+        d2h_stream.wait_event(cd)
+        with torch.cuda.stream(d2h_stream):
+            chs[b].copy_(B["c"], non_blocking=True)
+            sfhs[b].copy_(B["csf"], non_blocking=True)
+            dd = torch.cuda.Event()
+            dd.record(d2h_stream)
+            d2h_done[b] = dd
+
+    for i in range(2):
+        issue(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        issue(i)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = chs[0].numel() + sfhs[0].numel()
+    # plain host->device bandwidth of the largest input, for context
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record()
+    bufs[0][split].copy_(host[split], non_blocking=True)
+    h1.record()
+    torch.cuda.synchronize()
+    big = host[split].numel() * host[split].element_size()
+    out = {"value": round(world * fl / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_s * 1e3, 3),
+           "input": ("16384 bf16 tokens x 4096 + top-8 expert ids (int32); routing, amax and "
+                     "NVFP4 quantization of the gathered rows on the GPU"
+                     if form == "tokens" else
+                     "131072 pre-gathered bf16 rows x 4096 + group offsets"),
+           "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
+           "single_copy_h2d_GB/s": round(big / h0.elapsed_time(h1) / 1e6, 1)}
+    del bufs
+    return out
+
+
 def run_moeq(args, rank, world):
     from fp4_fp8_quantization_gb300 import moeq
     moeq.lib()
@@ -584,82 +720,11 @@ def run_moeq(args, rank, world):
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
                  "fused_gemm_swiglu_ms": round(t_f, 4)}
 
-    # end to end from pinned host buffers through the same calls; steps are
-    # pipelined: the host->device copy of step i+1 (split over several copy
-    # streams) overlaps the compute of step i, device->host copies run on
-    # their own stream, two device buffer sets alternate
-    xh = d["x"].cpu().pin_memory()
-    roh = d["ro"].cpu().pin_memory()
-    idh = d["ids"].cpu().pin_memory()
-    d_alt = dict(d)
-    for k in ("x", "ro", "ids", "so", "ts", "a", "asf", "c", "csf"):
-        d_alt[k] = torch.empty_like(d[k])
-    bufs = [d, d_alt]
-    chs = [torch.empty(d["c"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    sfhs = [torch.empty(d["csf"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    n_copy = 4
-    h2d_streams = [torch.cuda.Stream() for _ in range(n_copy)]
-    d2h_stream = torch.cuda.Stream()
-    comp = torch.cuda.current_stream()
-    comp_done, d2h_done = [None, None], [None, None]
-    e2e_steps = max(3, min(args.steps, 20))
-
-    def e2e_issue(i):
-        b = i % 2
-        B = bufs[b]
-        rows = B["x"].shape[0]
-        chunk = (rows + n_copy - 1) // n_copy
-        ready = []
-        for j, st in enumerate(h2d_streams):
-            if comp_done[b] is not None:       # step i-2 has finished reading buffer b
-                st.wait_event(comp_done[b])
-            with torch.cuda.stream(st):
-                r0, r1 = j * chunk, min(rows, (j + 1) * chunk)
-                B["x"][r0:r1].copy_(xh[r0:r1], non_blocking=True)
-                if j == 0:
-                    B["ro"].copy_(roh, non_blocking=True)
-                    B["ids"].copy_(idh, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(st)
-                ready.append(ev)
-        for ev in ready:
-            comp.wait_event(ev)
-        if d2h_done[b] is not None:             # outputs of step i-2 are on the host
-            comp.wait_event(d2h_done[b])
-        up_projection_step(B)
-        cd = torch.cuda.Event()
-        cd.record(comp)
-        comp_done[b] = cd
-        d2h_stream.wait_event(cd)
-        with torch.cuda.stream(d2h_stream):
-            chs[b].copy_(B["c"], non_blocking=True)
-            sfhs[b].copy_(B["csf"], non_blocking=True)
-            dd = torch.cuda.Event()
-            dd.record(d2h_stream)
-            d2h_done[b] = dd
-
-    for i in range(2):
-        e2e_issue(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_issue(i)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
-    # plain host->device bandwidth of the activations, for context
-    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h0.record()
-    d["x"].copy_(xh, non_blocking=True)
-    h1.record()
-    torch.cuda.synchronize()
-    h2d = xh.numel() * 2 + roh.numel() * 4 + idh.numel() * 4
-    d2h = chs[0].numel() + sfhs[0].numel()
-    e2e = {"value": round(world * fl / e2e_s / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_s * 1e3, 3),
-           "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
-           "single_copy_h2d_GB/s": round(xh.numel() * 2 / h0.elapsed_time(h1) / 1e6, 1)}
+    # end to end from pinned host memory: the layer's real input, the
+    # tokens and their top-k expert ids (routing and row gather on the GPU);
+    # and, for comparison, the 131072 pre-gathered rows of the timed step
+    e2e = run_e2e(d, args, world, fl, "tokens")
+    e2e["pregathered_rows_input"] = run_e2e(d, args, world, fl, "rows")
 
     extra = {}
     if rank == 0 and not args.no_parts:

@@ -192,3 +192,46 @@ def test_dispatch_full_size_sampled():
     assert np.array_equal(got, sc_ref)
     assert moeq.get_device_error() == 0
     note(choices=T * k, sampled_rows=int(len(sample)))
+
+
+def test_token_level_up_projection_equals_the_row_level_path():
+    """Routing + gathered amax / NVFP4 quantization + fused GEMM from the
+    tokens and their top-k ids gives the bytes of the row-level path run on
+    the materialised gathered rows (the two inputs of the benchmark's
+    end-to-end figures)."""
+    need_gpu()
+    moeq.clear_device_error()
+    T, K, E, k, I = 300, 512, 8, 4, 192
+    tok = synth.bf16_normal((T, K), 1.0, seed=71, device=DEV, outlier_p=0.01, outlier_scale=20.0)
+    tk = torch.from_numpy(synth.topk_ids(T, k, E, seed=72, zipf_s=0.7)).to(DEV)
+    n = T * k
+    rows = moeq.dispatch_scale_rows(T, k, E)
+    b = synth.random_fp4_packed((E, 2 * I, K // 2), seed=73, device=DEV)
+    bsf = synth.random_bytes(E * moeq.sf_bytes(2 * I, K // 16), 0x18, 0x28, seed=74, device=DEV)
+    es = synth.uniform((E,), 0.5, 2.0, seed=75, device=DEV)
+    ots = synth.uniform((E,), 0.05, 0.2, seed=76, device=DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    ro, eids, src, so = (torch.empty(E + 1, **i32), torch.empty(E, **i32), torch.empty(n, **i32),
+                         torch.empty(E + 1, **i32))
+    moeq.route_topk(tk, ro, eids, src, so)
+
+    def outputs():
+        u8z = lambda *shape: torch.zeros(*shape, dtype=torch.uint8, device=DEV)
+        return (torch.empty(E, device=DEV), u8z(n, K // 2), u8z(moeq.sf_bytes(rows, K // 16)),
+                u8z(n, I // 2), u8z(moeq.sf_bytes(rows, I // 16)))
+
+    ts1, a1, asf1, c1, csf1 = outputs()
+    moeq.grouped_amax_scale_gather(tok, src, k, ro, eids, ts1, E)
+    moeq.grouped_quantize_gather("nvfp4", tok, src, k, a1, asf1, ro, so, eids, ts1, E, rows)
+    moeq.grouped_matmul_swiglu(c1, csf1, a1, asf1, b, bsf, es, ots, ro, so, eids, I, K, rows)
+    x = tok[torch.div(src, k, rounding_mode="floor").long()].contiguous()
+    ts2, a2, asf2, c2, csf2 = outputs()
+    moeq.grouped_amax_scale(x, ro, eids, ts2, E)
+    moeq.grouped_quantize("nvfp4", x, a2, asf2, ro, so, eids, ts2, E, rows)
+    moeq.grouped_matmul_swiglu(c2, csf2, a2, asf2, b, bsf, es, ots, ro, so, eids, I, K, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(ts1.view(torch.int32), ts2.view(torch.int32))
+    assert torch.equal(a1, a2) and torch.equal(asf1, asf2)
+    assert torch.equal(c1, c2) and torch.equal(csf1, csf2)
+    assert (c1 != 0).float().mean() > 0.3
+    assert moeq.get_device_error() == 0
