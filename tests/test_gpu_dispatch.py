@@ -235,3 +235,22 @@ def test_token_level_up_projection_equals_the_row_level_path():
     assert torch.equal(c1, c2) and torch.equal(csf1, csf2)
     assert (c1 != 0).float().mean() > 0.3
     assert moeq.get_device_error() == 0
+
+
+@pytest.mark.parametrize("T,k,E", [(0, 2, 5), (1, 1, 1), (37, 1, 1), (5, 3, 1024)])
+def test_route_degenerate_sizes(T, k, E):
+    """No tokens, one expert, top-1, more experts than choices."""
+    need_gpu()
+    moeq.clear_device_error()
+    ids = _topk(T, k, E, seed=90 + T) if T else np.zeros((0, k), np.int32)
+    ro, eids, src, _ = D.route_topk(ids, E)
+    g_ro, g_eids, g_src, g_so = _route_gpu(ids, E)
+    assert np.array_equal(g_ro, ro)
+    assert np.array_equal(g_eids, eids)
+    assert np.array_equal(g_src[:len(src)], src)
+    assert np.array_equal(g_so, Q.padded_scale_offsets(ro))
+    if T == 0:
+        tok = torch.zeros((0, 256), dtype=torch.bfloat16, device=DEV)
+        out, sf, ro_d, _, so_d, _ = _dispatch_gpu(tok, ids, E)
+        assert int(ro_d[-1]) == 0 and int(so_d[-1]) == 0
+    assert moeq.get_device_error() == 0
