@@ -68,7 +68,7 @@ def parse_args():
     p.add_argument("--log", default=os.environ.get("MOEQ_METRICS_LOG"),
                    help="also append the JSON line to this file (default: $MOEQ_METRICS_LOG)")
     p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained",
-                                          "swiglu"],
+                                          "swiglu", "dispatch"],
                    help="run only --warmup + --steps launches of one kernel on a small case "
                         "(inputs larger than L2, under 1 GB) for a profiler; no JSON line")
     return p.parse_args()
@@ -767,7 +767,19 @@ def run_profile_case(args):
     from fp4_fp8_quantization_gb300 import moeq, synth
     dev = "cuda"
     u32 = lambda a: torch.from_numpy(np.asarray(a, np.uint32).view(np.int32)).to(dev)
-    if args.profile in ("fused", "chained", "quantize", "swiglu"):
+    if args.profile == "dispatch":
+        # single-rank MXFP4 dispatch: 16384 tokens x 4096, top-8 of 128 experts
+        tok = synth.bf16_normal((TOK4, K4), 1.0, seed=70, device=dev)
+        tk = torch.from_numpy(synth.topk_ids(TOK4, TOPK4, E4, seed=0)).to(dev)
+        n = TOK4 * TOPK4
+        rows = moeq.dispatch_scale_rows(TOK4, TOPK4, E4)
+        q = torch.empty((n, K4 // 2), dtype=torch.uint8, device=dev)
+        sf = torch.empty(moeq.sf_bytes(rows, K4 // 32), dtype=torch.uint8, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        ro, eids, src, so = (torch.empty(E4 + 1, **i32), torch.empty(E4, **i32),
+                             torch.empty(n, **i32), torch.empty(E4 + 1, **i32))
+        fn = lambda: moeq.dispatch_mxfp4(tok, tk, q, sf, ro, eids, src, so)
+    elif args.profile in ("fused", "chained", "quantize", "swiglu"):
         # 32 experts, 4096 tokens top-8 -> 32768 rows, K 4096, I 1536
         counts = synth.routing_counts(4096, 8, 32, seed=0)
         ro, ids = synth.ragged_groups(counts)
