@@ -46,6 +46,23 @@ def route_topk(topk_ids, num_experts):
     return row_offsets, np.arange(E, dtype=np.int32), src_info, dropped
 
 
+def topk_amax(tokens, topk_ids, num_experts):
+    """Per-expert amax from tokens and their top-k choices: amax_e = max |x_t|
+    over the tokens t with a choice of expert e (0 when there is none); ids
+    outside [0, E) are dropped.  The same set of values as the grouped amax
+    over the routed rows ("grouped_quantize_dynamic_scaled_fp4_async_kernel":
+    the per-expert tensor scale comes from the expert's rows)."""
+    x = np.asarray(tokens, dtype=np.float32)
+    ids = np.asarray(topk_ids, dtype=np.int64).reshape(x.shape[0], -1)
+    amax = np.zeros(int(num_experts), dtype=np.float32)
+    for t in range(x.shape[0]):
+        m = np.abs(x[t]).max() if x.shape[1] else np.float32(0)
+        for e in ids[t]:
+            if 0 <= e < num_experts:
+                amax[e] = max(amax[e], m)
+    return amax
+
+
 def slot_scale_offsets(num_experts, max_padded_m):
     """scales_offsets of the slot layout: group g starts at g * max_padded_M."""
     return (np.arange(int(num_experts) + 1, dtype=np.int64) * int(max_padded_m)).astype(np.uint32)

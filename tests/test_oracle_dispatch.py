@@ -78,3 +78,21 @@ def test_slot_layout_holds_the_same_scales_as_the_padded_layout():
                 pb = L.sf_offset(int(b["scales_offsets"][g]) + r - int(ro[g]), c, kv)
                 assert a["scales"][pa] == b["scales"][pb]
     assert b["scales"].size == L.physical_bytes(4 * 128, kv)
+
+
+def test_topk_amax_hand_case():
+    # token amaxes 3, 2, 4; expert 0 <- tokens 0, 2; 1 <- 0, 1; 2 <- 1, 2; 3 <- none
+    tok = np.array([[1, -3], [2, 0.5], [-4, 1]], np.float32)
+    amax = D.topk_amax(tok, [[0, 1], [1, 2], [2, 0]], 4)
+    assert amax.tolist() == [4.0, 3.0, 4.0, 0.0]
+    # an id outside the experts is dropped
+    assert D.topk_amax(tok, [[0, 9], [1, -1], [1, 0]], 2).tolist() == [4.0, 4.0]
+
+
+def test_topk_amax_equals_the_grouped_amax_of_the_routed_rows():
+    rng = np.random.default_rng(11)
+    tok = _tokens(50, 64, 12)
+    ids = np.stack([rng.choice(9, 3, replace=False) for _ in range(50)]).astype(np.int32)
+    ro, eids, src, _ = D.route_topk(ids, 9)
+    ref = Q.group_amax(tok[src // 3], ro, eids, 9)
+    assert np.array_equal(D.topk_amax(tok, ids, 9), ref)
