@@ -538,12 +538,12 @@ def run_reference(args, rank, world):
 
 
 def token_step(B, d):
-    """The up-projection from tokens and their top-k ids: routing, per-expert
-    amax and NVFP4 quantization of the gathered rows, fused GEMM + SwiGLU +
-    requant (the same GEMM work as up_projection_step)."""
+    """The up-projection from tokens and their top-k ids: per-expert amax
+    (each token read once), routing, NVFP4 quantization of the gathered rows,
+    fused GEMM + SwiGLU + requant (the same GEMM work as up_projection_step)."""
     from fp4_fp8_quantization_gb300 import moeq
+    moeq.grouped_amax_scale_topk(B["tok"], B["tk"], B["ts"], E4)   # each token read once
     moeq.route_topk(B["tk"], B["ro"], B["ids"], B["src"], B["so"])
-    moeq.grouped_amax_scale_gather(B["tok"], B["src"], TOPK4, B["ro"], B["ids"], B["ts"], E4)
     moeq.grouped_quantize_gather("nvfp4", B["tok"], B["src"], TOPK4, B["a"], B["asf"], B["ro"],
                                  B["so"], B["ids"], B["ts"], E4, B["rows"])
     moeq.grouped_matmul_swiglu(B["c"], B["csf"], B["a"], B["asf"], d["b"], d["bsf"], d["es"],
@@ -663,8 +663,8 @@ def run_e2e(d, args, world, fl, form):
     out = {"value": round(world * fl / e2e_s / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_s * 1e3, 3),
-           "input": ("16384 bf16 tokens x 4096 + top-8 expert ids (int32); routing, amax and "
-                     "NVFP4 quantization of the gathered rows on the GPU"
+           "input": ("16384 bf16 tokens x 4096 + top-8 expert ids (int32); per-expert amax, "
+                     "routing and NVFP4 quantization of the gathered rows on the GPU"
                      if form == "tokens" else
                      "131072 pre-gathered bf16 rows x 4096 + group offsets"),
            "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",

@@ -272,6 +272,25 @@ moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t
                                                slot_rows, err, stream));
 }
 
+moeq_status moeq_grouped_amax_scale_topk(const void *tokens, int64_t token_stride,
+                                         int64_t num_tokens, int64_t K, const int32_t *topk_ids,
+                                         int32_t top_k, float *tensor_scale_out,
+                                         int32_t num_experts, moeq_stream_t stream) {
+    if (num_tokens < 0 || top_k < 1 || num_experts < 1 || K <= 0 || K % 8 ||
+        token_stride < K || token_stride % 8 || !tensor_scale_out ||
+        !aligned16(tensor_scale_out))
+        return MOEQ_ERR_INVALID_ARG;
+    if (num_tokens >= ((int64_t)1 << 31) / top_k) return MOEQ_ERR_UNSUPPORTED;
+    if (num_tokens > 0 &&
+        (!tokens || !topk_ids || !aligned16(tokens) || !aligned16(topk_ids)))
+        return MOEQ_ERR_INVALID_ARG;
+    uint32_t *err = device_error_ptr();
+    if (!err) return cuda_status(cudaErrorInvalidDevice);
+    return cuda_status(moeq::launch_amax_scale_topk(tokens, token_stride, K, num_tokens, topk_ids,
+                                                    top_k, num_experts, tensor_scale_out, err,
+                                                    stream));
+}
+
 int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_experts,
                                  int32_t slot_rows) {
     if (num_tokens < 0 || top_k < 1 || num_experts < 1 || slot_rows < 0 ||

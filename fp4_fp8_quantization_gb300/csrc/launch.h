@@ -30,6 +30,11 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
                               const Gather &gt, float *tensor_scale_out, uint32_t *err,
                               cudaStream_t s);
 
+// Per-expert tensor scales from tokens and their top-k ids (each token read once).
+cudaError_t launch_amax_scale_topk(const void *in, int64_t stride, int64_t K, int64_t num_tokens,
+                                   const int32_t *topk_ids, int top_k, int num_experts,
+                                   float *tensor_scale_out, uint32_t *err, cudaStream_t s);
+
 cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,
                             uint8_t *scales, const float *tensor_scale, const GroupArgs &g,
                             const Gather &gt, uint32_t *err, cudaStream_t s);

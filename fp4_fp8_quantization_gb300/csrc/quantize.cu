@@ -292,6 +292,37 @@ __global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(co
         atomicMax(amax_bits + cur_e, cur_m << 16);
 }
 
+// Per-expert amax from tokens and their top-k expert ids: each token row is
+// read once and its max |x| goes to every expert it chose (atomic max on the
+// fp32 bits of the bf16 value), so the words equal amax_kernel's over the
+// routed rows without reading a token once per choice.  An id outside
+// [0, E) is skipped and sets MOEQ_DEVERR_BAD_EXPERT.
+__global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB)
+    amax_topk_kernel(const uint16_t *__restrict__ in, int64_t stride, int64_t K,
+                     int64_t num_tokens, const int32_t *__restrict__ topk, int top_k, int E,
+                     uint32_t *__restrict__ amax_bits, uint32_t *err, int rows_per_warp) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n16 = K / 8;
+    for (int64_t i = 0; i < rows_per_warp; ++i) {
+        const int64_t t = warp_id * rows_per_warp + i;
+        if (t >= num_tokens) break;
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + t * stride);
+        uint4 v[8];
+        row_first_loads(src, n16, lane, v);
+        const uint32_t m = row_abs_max(src, K, lane, v);
+        for (int j = lane; j < top_k; j += 32) {
+            const int e = __ldg(topk + t * top_k + j);
+            if (e < 0 || e >= E)
+                set_error(err, MOEQ_DEVERR_BAD_EXPERT);
+            else if (m && store_ok(e < E, err))
+                atomicMax(amax_bits + e, m << 16);
+        }
+    }
+}
+
 // Zeroes the per-expert amax words before amax_kernel's atomics.
 __global__ void zero_words_kernel(uint32_t *buf, int n) {
     pdl_wait();
@@ -691,6 +722,25 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(amax_finalize_kernel, eblocks, 256, 0, s, bits, (int)g.num_experts);
+}
+
+cudaError_t launch_amax_scale_topk(const void *in, int64_t stride, int64_t K, int64_t num_tokens,
+                                   const int32_t *topk_ids, int top_k, int num_experts,
+                                   float *tensor_scale_out, uint32_t *err, cudaStream_t s) {
+    uint32_t *bits = reinterpret_cast<uint32_t *>(tensor_scale_out);
+    const unsigned eblocks = (unsigned)((num_experts + 255) / 256);
+    cudaError_t e = launch_pdl(zero_words_kernel, eblocks, 256, 0, s, bits, num_experts);
+    if (e != cudaSuccess) return e;
+    if (num_tokens > 0) {
+        const int rows_per_warp = num_tokens >= 65536 ? MOEQ_A_RPW : 1;
+        const int64_t warps = (num_tokens + rows_per_warp - 1) / rows_per_warp;
+        const int64_t blocks = (warps + MOEQ_A_WARPS - 1) / MOEQ_A_WARPS;
+        e = launch_pdl(amax_topk_kernel, (unsigned)blocks, MOEQ_A_WARPS * 32, 0, s,
+                       reinterpret_cast<const uint16_t *>(in), stride, K, num_tokens, topk_ids,
+                       top_k, num_experts, bits, err, rows_per_warp);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(amax_finalize_kernel, eblocks, 256, 0, s, bits, num_experts);
 }
 
 cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, uint8_t *out,

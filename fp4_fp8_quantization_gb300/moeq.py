@@ -51,6 +51,7 @@ _SIGNATURES = {
     "moeq_interleave_gate_up": [_P, _P, _P, _I64, _I64, _I64, _P],
     "moeq_route_topk": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P],
     "moeq_dispatch_scale_rows": [_I64, _I32, _I32, _I32],
+    "moeq_grouped_amax_scale_topk": [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P],
     "moeq_dispatch_mxfp4": [_P, _I64, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P,
                             _I32, _P],
     "moeq_get_device_error": [_P, _U32P],
@@ -229,6 +230,18 @@ def route_topk(topk_ids, row_offsets, expert_ids, src_info, scales_offsets=None,
           topk_ids.shape[1], E, _ptr(row_offsets, _U32, "row_offsets"),
           _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(src_info, torch.int32, "src_info"),
           _ptr(scales_offsets, _U32, "scales_offsets"), slot_rows, _stream(stream))
+
+
+def grouped_amax_scale_topk(tokens, topk_ids, tensor_scale_out, num_experts, stream=None):
+    """Per-expert NVFP4 tensor scales from bf16 tokens [num_tokens, K] and
+    their top-k expert ids (int32 [num_tokens, top_k]); each token read once."""
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != tokens.shape[0]:
+        raise ValueError("topk_ids: expected [num_tokens, top_k]")
+    _call("moeq_grouped_amax_scale_topk", _ptr_rows(tokens, torch.bfloat16, "tokens"),
+          tokens.stride(0), tokens.shape[0], tokens.shape[1],
+          _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[1],
+          _ptr(tensor_scale_out, torch.float32, "tensor_scale_out"), num_experts,
+          _stream(stream))
 
 
 def dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows=0):

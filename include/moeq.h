@@ -358,6 +358,21 @@ moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t
                             int32_t *src_info, uint32_t *scales_offsets, int32_t slot_rows,
                             moeq_stream_t stream);
 
+/* Per-expert NVFP4 tensor scales from tokens and their top-k expert ids:
+ * tensor_scale_out[e] = amax_e / (6 * 448) (1 when amax_e == 0), amax_e the
+ * max |x| over the tokens with a choice of expert e -- the value
+ * moeq_grouped_amax_scale gives over the routed rows
+ * ("grouped_quantize_dynamic_scaled_fp4_async_kernel": the per-expert tensor
+ * scale), but each token row is read once instead of once per choice.
+ *   tokens      bf16 [num_tokens, K], row stride token_stride elements.
+ *   topk_ids    int32 [num_tokens, top_k] (device).
+ *   tensor_scale_out  fp32 [num_experts] (out).
+ * An id outside [0, num_experts) is skipped and sets MOEQ_DEVERR_BAD_EXPERT. */
+moeq_status moeq_grouped_amax_scale_topk(const void *tokens, int64_t token_stride,
+                                         int64_t num_tokens, int64_t K, const int32_t *topk_ids,
+                                         int32_t top_k, float *tensor_scale_out,
+                                         int32_t num_experts, moeq_stream_t stream);
+
 /* Scale rows that moeq_dispatch_mxfp4 needs: num_experts * slot_rows with
  * slot_rows > 0, else the largest possible padded total,
  * floor((num_tokens * top_k + 127 * num_experts) / 128) * 128.  Host only. */

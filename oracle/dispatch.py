@@ -53,7 +53,9 @@ def topk_amax(tokens, topk_ids, num_experts):
     over the routed rows ("grouped_quantize_dynamic_scaled_fp4_async_kernel":
     the per-expert tensor scale comes from the expert's rows)."""
     x = np.asarray(tokens, dtype=np.float32)
-    ids = np.asarray(topk_ids, dtype=np.int64).reshape(x.shape[0], -1)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    if ids.ndim != 2:
+        ids = ids.reshape(x.shape[0], -1)
     amax = np.zeros(int(num_experts), dtype=np.float32)
     for t in range(x.shape[0]):
         m = np.abs(x[t]).max() if x.shape[1] else np.float32(0)

@@ -195,9 +195,9 @@ def test_dispatch_full_size_sampled():
 
 
 def test_token_level_up_projection_equals_the_row_level_path():
-    """Routing + gathered amax / NVFP4 quantization + fused GEMM from the
-    tokens and their top-k ids gives the bytes of the row-level path run on
-    the materialised gathered rows (the two inputs of the benchmark's
+    """Token-major amax, routing, gathered NVFP4 quantization and fused GEMM
+    from the tokens and their top-k ids give the bytes of the row-level path
+    run on the materialised gathered rows (the two inputs of the benchmark's
     end-to-end figures)."""
     need_gpu()
     moeq.clear_device_error()
@@ -221,7 +221,7 @@ def test_token_level_up_projection_equals_the_row_level_path():
                 u8z(n, I // 2), u8z(moeq.sf_bytes(rows, I // 16)))
 
     ts1, a1, asf1, c1, csf1 = outputs()
-    moeq.grouped_amax_scale_gather(tok, src, k, ro, eids, ts1, E)
+    moeq.grouped_amax_scale_topk(tok, tk, ts1, E)
     moeq.grouped_quantize_gather("nvfp4", tok, src, k, a1, asf1, ro, so, eids, ts1, E, rows)
     moeq.grouped_matmul_swiglu(c1, csf1, a1, asf1, b, bsf, es, ots, ro, so, eids, I, K, rows)
     x = tok[torch.div(src, k, rounding_mode="floor").long()].contiguous()
@@ -254,3 +254,43 @@ def test_route_degenerate_sizes(T, k, E):
         out, sf, ro_d, _, so_d, _ = _dispatch_gpu(tok, ids, E)
         assert int(ro_d[-1]) == 0 and int(so_d[-1]) == 0
     assert moeq.get_device_error() == 0
+
+
+@pytest.mark.parametrize("T,k,E,K", [(300, 4, 8, 512), (16384, 8, 128, 4096), (100, 40, 64, 256),
+                                     (0, 2, 4, 256)])
+def test_topk_amax_matches_oracle_and_the_routed_amax(T, k, E, K):
+    """Per-expert tensor scales from the tokens and their top-k ids equal the
+    oracle's and those of the gathered amax over the routed rows, bit for bit."""
+    need_gpu()
+    moeq.clear_device_error()
+    tok = synth.bf16_normal((T, K), 1.0, seed=81 + T, device=DEV, outlier_p=0.002,
+                            outlier_scale=60.0)
+    ids = _topk(T, k, E, seed=82) if T else np.zeros((0, k), np.int32)
+    tk = torch.from_numpy(ids).to(DEV)
+    ts = torch.full((E,), -1.0, device=DEV)
+    moeq.grouped_amax_scale_topk(tok, tk, ts, E)
+    ref = Q.tensor_scale_from_amax(D.topk_amax(tok.float().cpu().numpy(), ids, E))
+    assert np.array_equal(ts.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    if T:
+        i32 = dict(dtype=torch.int32, device=DEV)
+        ro, eids, src = torch.empty(E + 1, **i32), torch.empty(E, **i32), torch.empty(T * k, **i32)
+        moeq.route_topk(tk, ro, eids, src)
+        ts2 = torch.empty(E, device=DEV)
+        moeq.grouped_amax_scale_gather(tok, src, k, ro, eids, ts2, E)
+        assert torch.equal(ts.view(torch.int32), ts2.view(torch.int32))
+    assert moeq.get_device_error() == 0
+
+
+def test_topk_amax_skips_invalid_ids():
+    need_gpu()
+    moeq.clear_device_error()
+    tok = synth.bf16_normal((64, 256), 1.0, seed=91, device=DEV)
+    ids = _topk(64, 2, 6, seed=92)
+    ids[3, 0] = -2
+    ids[40, 1] = 6
+    ts = torch.empty(6, device=DEV)
+    moeq.grouped_amax_scale_topk(tok, torch.from_numpy(ids).to(DEV), ts, 6)
+    ref = Q.tensor_scale_from_amax(D.topk_amax(tok.float().cpu().numpy(), ids, 6))
+    assert np.array_equal(ts.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert moeq.get_device_error() & moeq.DEVERR_BAD_EXPERT
+    moeq.clear_device_error()

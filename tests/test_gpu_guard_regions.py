@@ -164,5 +164,7 @@ def test_dispatch_entry_points_stay_in_their_buffers():
         out = g((T * k, H // 2), torch.uint8)
         sf = g((moeq.sf_bytes(rows, H // 32),), torch.uint8)
         moeq.dispatch_mxfp4(tok, ids, out, sf, ro, eids, src, so, slot)
+    ts = g((E,), torch.float32)
+    moeq.grouped_amax_scale_topk(tok, ids, ts, E)
     g.check()
     assert moeq.get_device_error() == 0
