@@ -364,15 +364,16 @@ def parts(pk, flush):
     src_d = torch.empty(n_rows, dtype=torch.int32, device=dev)
     so_dd = torch.empty(E4 + 1, dtype=torch.int32, device=dev)
     t_route = time_kernel(lambda: moeq.route_topk(tk, ro_dd, eid_d, src_d, so_dd), 20, batch=8)
+    dst_d = torch.empty(n_rows, dtype=torch.int32, device=dev)
     t_disp = time_kernel(lambda: moeq.dispatch_mxfp4(tok, tk, q_d, sf_d, ro_dd, eid_d, src_d,
-                                                     so_dd), 10)
+                                                     so_dd, dst_info=dst_d), 10)
     used_sf = int(so_dd[-1].item()) // 128 * (K4 // 32 // 4) * 512
     nbytes = tok.numel() * 2 + q_d.numel() + used_sf + tk.numel() * 4
     out["dispatch_mxfp4_16384tok_top8_128experts"] = {
         "route_us": round(t_route * 1e3, 2), "ms": round(t_disp, 4),
         "GB/s": round(nbytes / t_disp / 1e6, 1), "bytes": nbytes,
-        "bytes_note": "tokens read once + MXFP4 rows + used scale rows + top-k ids; the "
-                      "gather reads every token top_k times (1.07 GB of row reads)",
+        "bytes_note": "tokens read once (token-major quantization) + MXFP4 rows + used "
+                      "scale rows + top-k ids",
         "timing": "route: median of 20 batches of 8 calls; dispatch: mean of 10 calls"}
     del tok
     return out
@@ -538,14 +539,14 @@ def run_reference(args, rank, world):
 
 
 def token_step(B, d):
-    """The up-projection from tokens and their top-k ids: per-expert amax
-    (each token read once), routing, NVFP4 quantization of the gathered rows,
-    fused GEMM + SwiGLU + requant (the same GEMM work as up_projection_step)."""
+    """The up-projection from tokens and their top-k ids: per-expert amax and
+    NVFP4 quantization token-major (each token read once), routing, fused
+    GEMM + SwiGLU + requant (the same GEMM work as up_projection_step)."""
     from fp4_fp8_quantization_gb300 import moeq
     moeq.grouped_amax_scale_topk(B["tok"], B["tk"], B["ts"], E4)   # each token read once
-    moeq.route_topk(B["tk"], B["ro"], B["ids"], B["src"], B["so"])
-    moeq.grouped_quantize_gather("nvfp4", B["tok"], B["src"], TOPK4, B["a"], B["asf"], B["ro"],
-                                 B["so"], B["ids"], B["ts"], E4, B["rows"])
+    moeq.route_topk(B["tk"], B["ro"], B["ids"], B["src"], B["so"], dst_info=B["dst"])
+    moeq.quantize_topk("nvfp4", B["tok"], B["tk"], B["dst"], B["a"], B["asf"], B["ro"], B["so"],
+                       B["ts"], E4)                                 # each token read once
     moeq.grouped_matmul_swiglu(B["c"], B["csf"], B["a"], B["asf"], d["b"], d["bsf"], d["es"],
                                d["ots"], B["ro"], B["so"], B["ids"], I4, K4, B["rows"])
 
@@ -573,6 +574,7 @@ def run_e2e(d, args, world, fl, form):
                     "ro": torch.empty(E4 + 1, dtype=torch.int32, device="cuda"),
                     "ids": torch.empty(E4, dtype=torch.int32, device="cuda"),
                     "src": torch.empty(n, dtype=torch.int32, device="cuda"),
+                    "dst": torch.empty(n, dtype=torch.int32, device="cuda"),
                     "so": torch.empty(E4 + 1, dtype=torch.int32, device="cuda"),
                     "ts": torch.empty(E4, device="cuda"),
                     "a": torch.empty((n, K4 // 2), dtype=torch.uint8, device="cuda"),
@@ -664,7 +666,7 @@ def run_e2e(d, args, world, fl, form):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_s * 1e3, 3),
            "input": ("16384 bf16 tokens x 4096 + top-8 expert ids (int32); per-expert amax, "
-                     "routing and NVFP4 quantization of the gathered rows on the GPU"
+                     "routing and NVFP4 quantization of the routed rows on the GPU"
                      if form == "tokens" else
                      "131072 pre-gathered bf16 rows x 4096 + group offsets"),
            "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
@@ -778,7 +780,8 @@ def run_profile_case(args):
         i32 = dict(dtype=torch.int32, device=dev)
         ro, eids, src, so = (torch.empty(E4 + 1, **i32), torch.empty(E4, **i32),
                              torch.empty(n, **i32), torch.empty(E4 + 1, **i32))
-        fn = lambda: moeq.dispatch_mxfp4(tok, tk, q, sf, ro, eids, src, so)
+        dst = torch.empty(n, **i32)
+        fn = lambda: moeq.dispatch_mxfp4(tok, tk, q, sf, ro, eids, src, so, dst_info=dst)
     elif args.profile in ("fused", "chained", "quantize", "swiglu"):
         # 32 experts, 4096 tokens top-8 -> 32768 rows, K 4096, I 1536
         counts = synth.routing_counts(4096, 8, 32, seed=0)

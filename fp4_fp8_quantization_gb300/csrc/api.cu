@@ -244,7 +244,8 @@ moeq_status moeq_grouped_quantize_gather(moeq_format fmt, const void *in, int64_
 static moeq_status route_args_ok(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
                                  int32_t num_experts, const uint32_t *row_offsets,
                                  const int32_t *expert_ids, const int32_t *src_info,
-                                 const uint32_t *scales_offsets, int32_t slot_rows) {
+                                 const int32_t *dst_info, const uint32_t *scales_offsets,
+                                 int32_t slot_rows) {
     if (num_tokens < 0 || top_k < 1 || num_experts < 1 || slot_rows < 0 || slot_rows % 128)
         return MOEQ_ERR_INVALID_ARG;
     if (num_experts > moeq::kRouteMaxExperts || num_tokens >= ((int64_t)1 << 31) / top_k)
@@ -252,6 +253,7 @@ static moeq_status route_args_ok(const int32_t *topk_ids, int64_t num_tokens, in
     if (!row_offsets || !expert_ids || !aligned16(row_offsets) || !aligned16(expert_ids))
         return MOEQ_ERR_INVALID_ARG;
     if (scales_offsets && !aligned16(scales_offsets)) return MOEQ_ERR_INVALID_ARG;
+    if (dst_info && !aligned16(dst_info)) return MOEQ_ERR_INVALID_ARG;
     if (num_tokens > 0 &&
         (!topk_ids || !src_info || !aligned16(topk_ids) || !aligned16(src_info)))
         return MOEQ_ERR_INVALID_ARG;
@@ -260,16 +262,17 @@ static moeq_status route_args_ok(const int32_t *topk_ids, int64_t num_tokens, in
 
 moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
                             int32_t num_experts, uint32_t *row_offsets, int32_t *expert_ids,
-                            int32_t *src_info, uint32_t *scales_offsets, int32_t slot_rows,
-                            moeq_stream_t stream) {
+                            int32_t *src_info, int32_t *dst_info, uint32_t *scales_offsets,
+                            int32_t slot_rows, moeq_stream_t stream) {
     const moeq_status st = route_args_ok(topk_ids, num_tokens, top_k, num_experts, row_offsets,
-                                         expert_ids, src_info, scales_offsets, slot_rows);
+                                         expert_ids, src_info, dst_info, scales_offsets,
+                                         slot_rows);
     if (st != MOEQ_OK) return st;
     uint32_t *err = device_error_ptr();
     if (!err) return cuda_status(cudaErrorInvalidDevice);
     return cuda_status(moeq::launch_route_topk(topk_ids, num_tokens * top_k, num_experts,
-                                               row_offsets, expert_ids, src_info, scales_offsets,
-                                               slot_rows, err, stream));
+                                               row_offsets, expert_ids, src_info, dst_info,
+                                               scales_offsets, slot_rows, err, stream));
 }
 
 moeq_status moeq_grouped_amax_scale_topk(const void *tokens, int64_t token_stride,
@@ -301,31 +304,57 @@ int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_
     return (num_tokens * top_k + 127 * (int64_t)num_experts) / 128 * 128;
 }
 
+moeq_status moeq_quantize_topk(moeq_format fmt, const void *tokens, int64_t token_stride,
+                               int64_t num_tokens, int64_t K, const int32_t *topk_ids,
+                               int32_t top_k, const int32_t *dst_info,
+                               const uint32_t *row_offsets, const uint32_t *scales_offsets,
+                               const float *tensor_scale, int32_t num_experts, uint8_t *out,
+                               uint8_t *scales, int64_t scale_rows_total, moeq_stream_t stream) {
+    if (fmt != MOEQ_NVFP4 && fmt != MOEQ_MXFP4 && fmt != MOEQ_MXFP8) return MOEQ_ERR_INVALID_ARG;
+    if (num_tokens < 0 || top_k < 1 || num_experts < 1 || K <= 0 || K % 128 ||
+        token_stride < K || token_stride % 8 || scale_rows_total < 0 || scale_rows_total % 128)
+        return MOEQ_ERR_INVALID_ARG;
+    if (top_k > moeq::kTopkQuantMax || num_experts > moeq::kRouteMaxExperts ||
+        num_tokens >= ((int64_t)1 << 31) / top_k)
+        return MOEQ_ERR_UNSUPPORTED;
+    if (fmt == MOEQ_NVFP4 && !tensor_scale) return MOEQ_ERR_INVALID_ARG;
+    if (!row_offsets || !scales_offsets || !scales || !aligned16(scales)) return MOEQ_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!tokens || !topk_ids || !dst_info || !out || !aligned16(tokens) ||
+                           !aligned16(topk_ids) || !aligned16(dst_info) || !aligned16(out)))
+        return MOEQ_ERR_INVALID_ARG;
+    uint32_t *err = device_error_ptr();
+    if (!err) return cuda_status(cudaErrorInvalidDevice);
+    return cuda_status(moeq::launch_quantize_topk(
+        (int)fmt, tokens, token_stride, K, num_tokens, topk_ids, top_k, dst_info, row_offsets,
+        scales_offsets, tensor_scale, num_experts, num_tokens * top_k, scale_rows_total, out,
+        scales, err, stream));
+}
+
 moeq_status moeq_dispatch_mxfp4(const void *tokens, int64_t token_stride, int64_t num_tokens,
                                 int64_t hidden, const int32_t *topk_ids, int32_t top_k,
                                 int32_t num_experts, uint8_t *out, uint8_t *scales,
                                 int64_t scale_rows_total, uint32_t *row_offsets,
-                                int32_t *expert_ids, int32_t *src_info,
+                                int32_t *expert_ids, int32_t *src_info, int32_t *dst_info,
                                 uint32_t *scales_offsets, int32_t slot_rows,
                                 moeq_stream_t stream) {
     moeq_status st = route_args_ok(topk_ids, num_tokens, top_k, num_experts, row_offsets,
-                                   expert_ids, src_info, scales_offsets, slot_rows);
+                                   expert_ids, src_info, dst_info, scales_offsets, slot_rows);
     if (st != MOEQ_OK) return st;
     // every check of the quantization step before anything is launched
     if (!scales_offsets || hidden <= 0 || hidden % 128 || token_stride < hidden ||
-        token_stride % 8 || scale_rows_total % 128 ||
+        token_stride % 8 || scale_rows_total % 128 || !scales || !aligned16(scales) ||
         scale_rows_total < moeq_dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows))
         return MOEQ_ERR_INVALID_ARG;
-    if (num_tokens > 0 && (!tokens || !out || !scales || !aligned16(tokens) || !aligned16(out) ||
-                           !aligned16(scales)))
+    if (top_k > moeq::kTopkQuantMax) return MOEQ_ERR_UNSUPPORTED;
+    if (num_tokens > 0 && (!tokens || !out || !dst_info || !aligned16(tokens) || !aligned16(out)))
         return MOEQ_ERR_INVALID_ARG;
     st = moeq_route_topk(topk_ids, num_tokens, top_k, num_experts, row_offsets, expert_ids,
-                         src_info, scales_offsets, slot_rows, stream);
-    if (st != MOEQ_OK || num_tokens == 0) return st;
-    const moeq::Gather gt{src_info, top_k, num_tokens};
-    return quantize_impl(MOEQ_MXFP4, tokens, token_stride, num_tokens * top_k, hidden, out,
-                         scales, scale_rows_total, row_offsets, scales_offsets, expert_ids,
-                         nullptr, num_experts, num_experts, gt, stream);
+                         src_info, dst_info, scales_offsets, slot_rows, stream);
+    if (st != MOEQ_OK) return st;
+    // token-major: each token read and quantized once, stored to its routed rows
+    return moeq_quantize_topk(MOEQ_MXFP4, tokens, token_stride, num_tokens, hidden, topk_ids,
+                              top_k, dst_info, row_offsets, scales_offsets, nullptr, num_experts,
+                              out, scales, scale_rows_total, stream);
 }
 
 moeq_status moeq_grouped_matmul_rowwise_fp8(void *c, const uint8_t *a, const uint8_t *b,

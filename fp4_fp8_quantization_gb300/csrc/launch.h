@@ -39,6 +39,16 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
                             uint8_t *scales, const float *tensor_scale, const GroupArgs &g,
                             const Gather &gt, uint32_t *err, cudaStream_t s);
 
+// Token-major quantization of routed tokens (each token read once, written
+// to every routed row dst_info[t * top_k + j]); top_k <= kTopkQuantMax.
+constexpr int kTopkQuantMax = 8;
+cudaError_t launch_quantize_topk(int fmt, const void *in, int64_t stride, int64_t K,
+                                 int64_t num_tokens, const int32_t *topk_ids, int top_k,
+                                 const int32_t *dst_info, const uint32_t *row_offsets,
+                                 const uint32_t *scales_offsets, const float *tensor_scale,
+                                 int num_experts, int64_t total_rows, int64_t scale_rows_total,
+                                 uint8_t *out, uint8_t *scales, uint32_t *err, cudaStream_t s);
+
 cudaError_t launch_padded_offsets(const uint32_t *row_offsets, uint32_t *scales_offsets,
                                   int32_t num_groups, cudaStream_t s);
 
@@ -62,8 +72,8 @@ cudaError_t launch_interleave_rows(uint8_t *out, const uint8_t *gate, const uint
 constexpr int kRouteMaxExperts = 1024;
 cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int num_experts,
                               uint32_t *row_offsets, int32_t *expert_ids, int32_t *src_info,
-                              uint32_t *scales_offsets, int slot_rows, uint32_t *err,
-                              cudaStream_t s);
+                              int32_t *dst_info, uint32_t *scales_offsets, int slot_rows,
+                              uint32_t *err, cudaStream_t s);
 
 // Grouped GEMMs.  kind: 0 = FP8 rowwise, 1 = NVFP4 block-scaled,
 // 2 = MXFP8 block-scaled, 3 = MXFP4 block-scaled.  epi: 0 = bf16 out,

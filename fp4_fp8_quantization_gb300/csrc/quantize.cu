@@ -551,6 +551,206 @@ __global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB) quantize_kernel(Qua
     }
 }
 
+// ------------------------------------------- token-major quantization
+
+// Token-major form of the gathered quantizer for routed tokens: one warp per
+// token reads the token's row once and writes every routed copy of it
+// (routed row dst[t * top_k + j] of expert topk[t * top_k + j]), with the
+// same per-row arithmetic as quantize_kernel on the gathered rows, so the
+// bytes are those of moeq_grouped_quantize_gather with indices = src_info
+// and divisor = top_k.  MX formats: one quantization per block, stored
+// top_k times.  NVFP4: the block amax and the loads are shared, the scale
+// code and the element codes use each expert's tensor scale (per-choice
+// multiplier tables in shared memory).  Padding scale rows are zeroed by
+// zero_padding_scale_rows_kernel.
+constexpr int kTopkMax = 8;
+
+struct TopkQuantParams {
+    const uint16_t *in;
+    int64_t stride, K, num_tokens;
+    const int32_t *topk, *dst;  // [num_tokens * top_k]
+    int top_k, E;
+    const uint32_t *ro, *so;    // [E + 1]
+    const float *tensor_scale;  // NVFP4
+    int64_t total_rows, scale_rows_total;
+    uint8_t *out, *scales;
+    uint32_t *err;
+};
+
+// Routed row and logical scale row of choice (t, j), -1 when the choice is
+// dropped or its group cannot hold its scale rows (then flagged).
+__device__ __forceinline__ void topk_choice(const TopkQuantParams &p, int64_t i, int64_t &row,
+                                            int64_t &prow, int &e) {
+    row = prow = -1;
+    e = __ldg(p.topk + i);
+    const int pos = __ldg(p.dst + i);
+    if (e < 0 || e >= p.E || pos < 0) return;  // dropped by the router (already flagged)
+    const uint32_t r0 = __ldg(p.ro + e), r1 = __ldg(p.ro + e + 1);
+    const uint32_t s0 = __ldg(p.so + e), s1 = __ldg(p.so + e + 1);
+    if (r1 < r0 || (int64_t)r1 > p.total_rows || (uint32_t)pos < r0 || (uint32_t)pos >= r1) {
+        set_error(p.err, MOEQ_DEVERR_BAD_OFFSETS);
+        return;
+    }
+    const uint32_t need = (r1 - r0 + 127u) & ~127u;
+    if ((s0 & 127u) || s1 < s0 || s1 - s0 < need || (int64_t)s1 > p.scale_rows_total) {
+        set_error(p.err, MOEQ_DEVERR_SCALE_ROWS);
+        return;
+    }
+    row = pos;
+    prow = (int64_t)s0 + (pos - r0);
+}
+
+template <int FMT, bool A32>
+__global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB)
+    quantize_topk_kernel(TopkQuantParams p) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float r_table[FMT == 0 ? kQWarps : 1][FMT == 0 ? kTopkMax : 1][128];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int64_t t = (int64_t)blockIdx.x * kQWarps + wid;
+    if (t >= p.num_tokens) return;
+    // lane j < top_k holds choice j's routed row, scale row and inverse scale
+    int64_t my_row = -1, my_prow = -1;
+    float my_inv = 0.0f;
+    if (lane < p.top_k) {
+        int e;
+        topk_choice(p, t * p.top_k + lane, my_row, my_prow, e);
+        if (FMT == 0 && my_row >= 0) my_inv = __fdiv_rn(1.0f, __ldg(p.tensor_scale + e));
+    }
+    if (FMT == 0) {
+        for (int j = 0; j < p.top_k; ++j) {
+            const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, j);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                r_table[wid][j][lane * 4 + c] = nvfp4_r_entry(lane * 4 + c, inv);
+        }
+        __syncwarp();
+    }
+    constexpr int V = FMT == 0 ? 16 : 32;
+    const int64_t kv_atoms = p.K / V / 4;
+    const int64_t ob = FMT == 2 ? p.K : p.K / 2;  // output bytes per row
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + t * p.stride);
+    const int nsteps = (int)((p.K + 511) / 512);
+    const int lanes_last = (int)(p.K / 16 - (int64_t)(nsteps - 1) * 32);
+    constexpr int U = 2;  // 32-byte loads in flight per lane
+    for (int s0 = 0; s0 < nsteps; s0 += U) {
+        uint32_t w[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            const int s = s0 + u;
+            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u;
+            if (s >= nsteps) break;
+            const bool active = s < nsteps - 1 || lane < lanes_last;
+            uint32_t mb = bf16_abs_max16(w[u]);
+            if (FMT == 0) {
+                float x[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[h][2 * i] = bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu);
+                        x[h][2 * i + 1] = __uint_as_float(w[u][4 * h + i] & 0xFFFF0000u);
+                    }
+                }
+                const float mf = bf16_bits_to_f32(mb);
+                for (int j = 0; j < p.top_k; ++j) {
+                    const int64_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+                    const int64_t prow = __shfl_sync(0xFFFFFFFFu, my_prow, j);
+                    const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, j);
+                    if (row < 0) continue;  // the same for every lane
+                    const uint32_t code = nvfp4_block_scale_code(mf, inv).code;
+                    const float r = r_table[wid][j][code];
+                    const uint32_t c0 = nvfp4_codes8(x[0], r), c1 = nvfp4_codes8(x[1], r);
+                    const uint32_t word = gather4(code, lane, 1);
+                    if (!active) continue;
+                    if (!store_ok(row < p.total_rows && prow < p.scale_rows_total, p.err))
+                        continue;
+                    reinterpret_cast<uint2 *>(p.out + row * ob)[s * 32 + lane] = make_uint2(c0, c1);
+                    if ((lane & 3) == 0)
+                        *reinterpret_cast<uint32_t *>(
+                            p.scales + sf_word_offset(prow, s * 8 + (lane >> 2), kv_atoms)) = word;
+                }
+            } else {
+                mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));  // lanes 2j, 2j+1
+                constexpr int emax = FMT == 2 ? 8 : 2;
+                uint32_t code = 0;
+                float f = 0.0f;
+                if (mb != 0) {
+                    int cs = bf16_floor_log2(mb) - emax + 127;
+                    cs = min(max(cs, 0), 254);
+                    code = (uint32_t)cs;
+                    f = __uint_as_float((uint32_t)(254 - cs) << 23);  // 2^(127-c)
+                }
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float y[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        y[2 * i] = __fmul_rn(bf16_bits_to_f32(w[u][4 * h + i] & 0xFFFFu), f);
+                        y[2 * i + 1] = __fmul_rn(__uint_as_float(w[u][4 * h + i] & 0xFFFF0000u), f);
+                    }
+                    if (FMT == 2) {
+                        o[2 * h] = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+                        o[2 * h + 1] = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
+                    } else {
+                        o[h] = e2m1x8(y);
+                    }
+                }
+                if (mb == 0) o[0] = o[1] = o[2] = o[3] = 0u;  // all-zero block: +0 codes
+                const uint32_t word = gather4(code, lane, 2);
+                for (int j = 0; j < p.top_k; ++j) {
+                    const int64_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+                    const int64_t prow = __shfl_sync(0xFFFFFFFFu, my_prow, j);
+                    if (row < 0 || !active) continue;
+                    if (!store_ok(row < p.total_rows && prow < p.scale_rows_total, p.err))
+                        continue;
+                    if (FMT == 2)
+                        st_global_v4(p.out + row * ob + (int64_t)s * 512 + lane * 16, o[0], o[1],
+                                     o[2], o[3]);
+                    else
+                        reinterpret_cast<uint2 *>(p.out + row * ob)[s * 32 + lane] =
+                            make_uint2(o[0], o[1]);
+                    if ((lane & 7) == 0)
+                        *reinterpret_cast<uint32_t *>(
+                            p.scales + sf_word_offset(prow, s * 4 + (lane >> 3), kv_atoms)) = word;
+                }
+            }
+        }
+    }
+}
+
+// Zero scale words of every group's padding rows, [so[e] + r_e,
+// so[e] + ceil128(r_e)), for groups whose scale rows fit (as the grouped
+// quantizer writes them); one CTA per group.
+__global__ void zero_padding_scale_rows_kernel(const uint32_t *ro, const uint32_t *so, int E,
+                                               int64_t total_rows, int64_t scale_rows_total,
+                                               int64_t kv_atoms, uint8_t *scales, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
+    const int e = blockIdx.x;
+    if (e >= E) return;
+    const uint32_t r0 = __ldg(ro + e), r1 = __ldg(ro + e + 1);
+    const uint32_t s0 = __ldg(so + e), s1 = __ldg(so + e + 1);
+    if (r1 < r0 || (int64_t)r1 > total_rows) return;
+    const uint32_t rg = r1 - r0, need = (rg + 127u) & ~127u;
+    if ((s0 & 127u) || s1 < s0 || s1 - s0 < need || (int64_t)s1 > scale_rows_total) return;
+    const int64_t nwords = (int64_t)(need - rg) * kv_atoms;
+    for (int64_t k = threadIdx.x; k < nwords; k += blockDim.x) {
+        const int64_t prow = (int64_t)s0 + rg + k / kv_atoms;
+        if (store_ok(prow < scale_rows_total, err))
+            *reinterpret_cast<uint32_t *>(scales + sf_word_offset(prow, k % kv_atoms, kv_atoms)) = 0u;
+    }
+}
+
 // --------------------------------------------- chained SwiGLU + NVFP4
 
 struct SwigluParams {
@@ -756,6 +956,29 @@ cudaError_t launch_quantize(int fmt, const void *in, int64_t stride, int64_t K, 
         fmt == 0 ? (a32 ? quantize_kernel<0, true> : quantize_kernel<0, false>)
         : fmt == 1 ? (a32 ? quantize_kernel<1, true> : quantize_kernel<1, false>)
                    : (a32 ? quantize_kernel<2, true> : quantize_kernel<2, false>);
+    return launch_pdl(kern, (unsigned)blocks, kQWarps * 32, 0, s, p);
+}
+
+cudaError_t launch_quantize_topk(int fmt, const void *in, int64_t stride, int64_t K,
+                                 int64_t num_tokens, const int32_t *topk_ids, int top_k,
+                                 const int32_t *dst_info, const uint32_t *row_offsets,
+                                 const uint32_t *scales_offsets, const float *tensor_scale,
+                                 int num_experts, int64_t total_rows, int64_t scale_rows_total,
+                                 uint8_t *out, uint8_t *scales, uint32_t *err, cudaStream_t s) {
+    const int64_t kv_atoms = K / (fmt == 0 ? 16 : 32) / 4;
+    cudaError_t e = launch_pdl(zero_padding_scale_rows_kernel, (unsigned)num_experts, 256, 0, s,
+                               row_offsets, scales_offsets, num_experts, total_rows,
+                               scale_rows_total, kv_atoms, scales, err);
+    if (e != cudaSuccess || num_tokens == 0) return e;
+    TopkQuantParams p{reinterpret_cast<const uint16_t *>(in), stride, K, num_tokens, topk_ids,
+                      dst_info, top_k, num_experts, row_offsets, scales_offsets, tensor_scale,
+                      total_rows, scale_rows_total, out, scales, err};
+    const int64_t blocks = (num_tokens + kQWarps - 1) / kQWarps;
+    const bool a32 = (reinterpret_cast<uintptr_t>(in) % 32 == 0) && (stride % 16 == 0);
+    void (*kern)(TopkQuantParams) =
+        fmt == 0 ? (a32 ? quantize_topk_kernel<0, true> : quantize_topk_kernel<0, false>)
+        : fmt == 1 ? (a32 ? quantize_topk_kernel<1, true> : quantize_topk_kernel<1, false>)
+                   : (a32 ? quantize_topk_kernel<2, true> : quantize_topk_kernel<2, false>);
     return launch_pdl(kern, (unsigned)blocks, kQWarps * 32, 0, s, p);
 }
 

@@ -14,7 +14,8 @@
 // 2 walks each segment in order, 32 choices at a time, and ranks equal
 // experts within the warp (match.any): a stable order with no atomics on
 // the positions.  The scattered 4-byte stores of src_info are spread over
-// the cluster's SMs.
+// the cluster's SMs; the inverse map dst_info (the row of each choice) is
+// written in choice order.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -67,8 +68,8 @@ __device__ __forceinline__ void block_exclusive_scan2(uint32_t &v0, uint32_t &v1
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_topk_kernel(const int32_t *__restrict__ ids, int64_t n, int E, uint32_t *row_offsets,
-                      int32_t *expert_ids, int32_t *src_info, uint32_t *scales_offsets,
-                      int slot_rows, uint32_t *err) {
+                      int32_t *expert_ids, int32_t *src_info, int32_t *dst_info,
+                      uint32_t *scales_offsets, int slot_rows, uint32_t *err) {
     // [kRouteWarps][E] per-warp histograms, then [E] chunk counts (read by
     // the other CTAs), [E] expert totals, [E] this chunk's offset in each group
     extern __shared__ uint32_t hist[];
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             if (ok && (peers & lt) == 0) h[e] += __popc(peers);  // the group's lowest lane
             __syncwarp();
             if (ok && store_ok(pos < rows_total, err)) src_info[pos] = (int32_t)i;
+            if (dst_info && i < s1) dst_info[i] = ok ? (int32_t)pos : -1;
         }
     }
 }
@@ -200,8 +202,8 @@ size_t route_smem_bytes(int num_experts) {
 
 cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int num_experts,
                               uint32_t *row_offsets, int32_t *expert_ids, int32_t *src_info,
-                              uint32_t *scales_offsets, int slot_rows, uint32_t *err,
-                              cudaStream_t s) {
+                              int32_t *dst_info, uint32_t *scales_offsets, int slot_rows,
+                              uint32_t *err, cudaStream_t s) {
     const size_t smem = route_smem_bytes(num_experts);
     // per device, the largest dynamic shared memory set so far
     static size_t smem_set[64] = {0};
@@ -230,7 +232,8 @@ cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, route_topk_kernel, topk_ids, num_choices, num_experts,
-                              row_offsets, expert_ids, src_info, scales_offsets, slot_rows, err);
+                              row_offsets, expert_ids, src_info, dst_info, scales_offsets,
+                              slot_rows, err);
 }
 
 }  // namespace moeq

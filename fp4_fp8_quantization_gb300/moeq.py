@@ -49,11 +49,13 @@ _SIGNATURES = {
     "moeq_sf_swizzle": [_P, _P, _I64, _I64, _I64, _P],
     "moeq_sf_unswizzle": [_P, _P, _I64, _I64, _I64, _P],
     "moeq_interleave_gate_up": [_P, _P, _P, _I64, _I64, _I64, _P],
-    "moeq_route_topk": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P],
+    "moeq_route_topk": [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P],
+    "moeq_quantize_topk": [_I32, _P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _I32, _P, _P,
+                           _I64, _P],
     "moeq_dispatch_scale_rows": [_I64, _I32, _I32, _I32],
     "moeq_grouped_amax_scale_topk": [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P],
     "moeq_dispatch_mxfp4": [_P, _I64, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P,
-                            _I32, _P],
+                            _P, _I32, _P],
     "moeq_get_device_error": [_P, _U32P],
     "moeq_clear_device_error": [_P],
     "moeq_last_cuda_error": [],
@@ -216,11 +218,12 @@ def interleave_gate_up(out, gate, up, stream=None):
 
 
 def route_topk(topk_ids, row_offsets, expert_ids, src_info, scales_offsets=None, slot_rows=0,
-               stream=None):
+               stream=None, dst_info=None):
     """Routes the choices of topk_ids (int32 [num_tokens, top_k]) to the
     groups of their experts: row_offsets (int32/uint32 [E + 1]), expert_ids
     (int32 [E]), src_info (int32 [num_tokens * top_k]) and, if given,
-    scales_offsets ([E + 1]: padded, or slots of slot_rows rows)."""
+    scales_offsets ([E + 1]: padded, or slots of slot_rows rows) and
+    dst_info (int32 [num_tokens * top_k], the row of each choice)."""
     if topk_ids.dim() != 2:
         raise ValueError("topk_ids: expected [num_tokens, top_k]")
     E = expert_ids.numel()
@@ -229,7 +232,8 @@ def route_topk(topk_ids, row_offsets, expert_ids, src_info, scales_offsets=None,
     _call("moeq_route_topk", _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[0],
           topk_ids.shape[1], E, _ptr(row_offsets, _U32, "row_offsets"),
           _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(src_info, torch.int32, "src_info"),
-          _ptr(scales_offsets, _U32, "scales_offsets"), slot_rows, _stream(stream))
+          _ptr(dst_info, torch.int32, "dst_info"), _ptr(scales_offsets, _U32, "scales_offsets"),
+          slot_rows, _stream(stream))
 
 
 def grouped_amax_scale_topk(tokens, topk_ids, tensor_scale_out, num_experts, stream=None):
@@ -252,8 +256,28 @@ def dispatch_scale_rows(num_tokens, top_k, num_experts, slot_rows=0):
     return n
 
 
+def quantize_topk(fmt, tokens, topk_ids, dst_info, out, scales, row_offsets, scales_offsets,
+                  tensor_scale, num_experts, stream=None):
+    """Token-major quantization of routed tokens (the bytes of
+    grouped_quantize_gather on the routed rows, each token read once):
+    tokens bf16 [num_tokens, K]; topk_ids int32 [num_tokens, top_k];
+    dst_info, row_offsets, scales_offsets from route_topk; out
+    [num_tokens * top_k, K / 2] (FP4) or [.., K] (MXFP8)."""
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != tokens.shape[0]:
+        raise ValueError("topk_ids: expected [num_tokens, top_k]")
+    T, K = tokens.shape
+    v = 16 if fmt == "nvfp4" else 32
+    rows = scales.numel() // max(1, sf_bytes(128, K // v)) * 128
+    _call("moeq_quantize_topk", _fmt(fmt), _ptr_rows(tokens, torch.bfloat16, "tokens"),
+          tokens.stride(0), T, K, _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[1],
+          _ptr(dst_info, torch.int32, "dst_info"), _ptr(row_offsets, _U32, "row_offsets"),
+          _ptr(scales_offsets, _U32, "scales_offsets"),
+          _ptr(tensor_scale, torch.float32, "tensor_scale"), num_experts,
+          _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"), rows, _stream(stream))
+
+
 def dispatch_mxfp4(tokens, topk_ids, out, scales, row_offsets, expert_ids, src_info,
-                   scales_offsets, slot_rows=0, stream=None):
+                   scales_offsets, slot_rows=0, stream=None, dst_info=None):
     """Single-rank expert dispatch: route_topk, then MXFP4 quantization of
     the routed rows (row r is token src_info[r] // top_k).  tokens bf16
     [num_tokens, hidden]; out uint8 [num_tokens * top_k, hidden / 2]; scales
@@ -266,12 +290,14 @@ def dispatch_mxfp4(tokens, topk_ids, out, scales, row_offsets, expert_ids, src_i
     if out.numel() < topk_ids.numel() * (H // 2) or row_offsets.numel() != E + 1:
         raise ValueError("out [num_tokens * top_k, hidden / 2] and row_offsets [E + 1] expected")
     rows = scales.numel() // max(1, sf_bytes(128, H // 32)) * 128
+    if dst_info is None:   # the inverse routing map, device memory owned by the caller
+        dst_info = torch.empty(topk_ids.numel(), dtype=torch.int32, device=tokens.device)
     _call("moeq_dispatch_mxfp4", _ptr_rows(tokens, torch.bfloat16, "tokens"), tokens.stride(0),
           T, H, _ptr(topk_ids, torch.int32, "topk_ids"), topk_ids.shape[1], E,
           _ptr(out, _U8, "out"), _ptr(scales, _U8, "scales"), rows,
           _ptr(row_offsets, _U32, "row_offsets"), _ptr(expert_ids, torch.int32, "expert_ids"),
-          _ptr(src_info, torch.int32, "src_info"), _ptr(scales_offsets, _U32, "scales_offsets"),
-          slot_rows, _stream(stream))
+          _ptr(src_info, torch.int32, "src_info"), _ptr(dst_info, torch.int32, "dst_info"),
+          _ptr(scales_offsets, _U32, "scales_offsets"), slot_rows, _stream(stream))
 
 
 def grouped_matmul_rowwise_fp8(c, a, b, a_scales, b_scales, a_offsets, expert_ids,

@@ -343,6 +343,9 @@ moeq_status moeq_interleave_gate_up(uint8_t *out, const uint8_t *gate, const uin
  *   src_info        int32 [num_tokens * top_k] (out): row r holds choice
  *                   src_info[r] (token src_info[r] / top_k); entries past
  *                   row_offsets[num_experts] are not written.
+ *   dst_info        int32 [num_tokens * top_k] (out, may be NULL): the row of
+ *                   choice i (the inverse of src_info), -1 for a dropped
+ *                   choice.
  *   scales_offsets  u32 [num_experts + 1] (out, may be NULL): with
  *                   slot_rows == 0 the padded prefix of ceil(r_e / 128) * 128
  *                   (as moeq_padded_scale_offsets); with slot_rows > 0 (a
@@ -355,8 +358,31 @@ moeq_status moeq_interleave_gate_up(uint8_t *out, const uint8_t *gate, const uin
  * memory besides the outputs. */
 moeq_status moeq_route_topk(const int32_t *topk_ids, int64_t num_tokens, int32_t top_k,
                             int32_t num_experts, uint32_t *row_offsets, int32_t *expert_ids,
-                            int32_t *src_info, uint32_t *scales_offsets, int32_t slot_rows,
-                            moeq_stream_t stream);
+                            int32_t *src_info, int32_t *dst_info, uint32_t *scales_offsets,
+                            int32_t slot_rows, moeq_stream_t stream);
+
+/* Token-major quantization of routed tokens: the bytes of
+ * moeq_grouped_quantize_gather(fmt, tokens, indices = src_info,
+ * indices_divisor = top_k, groups = all num_experts experts, row_offsets,
+ * scales_offsets, expert_ids = 0..E-1, tensor_scale) -- the same NVFP4 /
+ * MXFP4 / MXFP8 rule per routed row, padding scale rows zero -- but each
+ * token row is read once and written to its routed rows dst_info[t * top_k
+ * + j] (MX formats quantize it once; NVFP4 shares the loads and block amax
+ * across the choices' tensor scales).
+ *   tokens       bf16 [num_tokens, K], row stride token_stride; K % 128 == 0.
+ *   topk_ids, dst_info  int32 [num_tokens * top_k] (from moeq_route_topk).
+ *   row_offsets, scales_offsets  u32 [num_experts + 1] (from moeq_route_topk).
+ *   tensor_scale fp32 [num_experts] raw per-expert scales (NVFP4 only).
+ *   out          [num_tokens * top_k, K / 2] (FP4) or [.., K] (MXFP8).
+ *   scales       tiled block scales of scale_rows_total logical rows.
+ * top_k <= 8 (else MOEQ_ERR_UNSUPPORTED).  A group whose scale rows do not
+ * fit is skipped and sets MOEQ_DEVERR_SCALE_ROWS. */
+moeq_status moeq_quantize_topk(moeq_format fmt, const void *tokens, int64_t token_stride,
+                               int64_t num_tokens, int64_t K, const int32_t *topk_ids,
+                               int32_t top_k, const int32_t *dst_info,
+                               const uint32_t *row_offsets, const uint32_t *scales_offsets,
+                               const float *tensor_scale, int32_t num_experts, uint8_t *out,
+                               uint8_t *scales, int64_t scale_rows_total, moeq_stream_t stream);
 
 /* Per-expert NVFP4 tensor scales from tokens and their top-k expert ids:
  * tensor_scale_out[e] = amax_e / (6 * 448) (1 when amax_e == 0), amax_e the
@@ -380,8 +406,8 @@ int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_
                                  int32_t slot_rows);
 
 /* moeq_route_topk, then MXFP4 quantization of the routed rows (routed row r
- * is token src_info[r] / top_k; moeq_grouped_quantize_gather with
- * indices = src_info, indices_divisor = top_k), in stream order.
+ * is token src_info[r] / top_k), token-major (moeq_quantize_topk: each
+ * token quantized once and stored to its top_k rows), in stream order.
  *   tokens          bf16 [num_tokens, hidden], row stride token_stride
  *                   elements; hidden a multiple of 128.
  *   out             uint8 [num_tokens * top_k, hidden / 2] packed E2M1
@@ -389,15 +415,16 @@ int64_t moeq_dispatch_scale_rows(int64_t num_tokens, int32_t top_k, int32_t num_
  *   scales          tiled E8M0 block scales of scale_rows_total logical rows
  *                   of hidden / 32 scales; scale_rows_total >=
  *                   moeq_dispatch_scale_rows(...) and a multiple of 128.
- *   row_offsets, expert_ids, src_info, scales_offsets: as moeq_route_topk
- *                   (scales_offsets required here).
+ *   row_offsets, expert_ids, src_info, dst_info, scales_offsets: as
+ *                   moeq_route_topk (dst_info and scales_offsets required
+ *                   here).  top_k <= 8.
  * With slot_rows > 0 a group larger than slot_rows is not quantized and
  * sets MOEQ_DEVERR_SCALE_ROWS. */
 moeq_status moeq_dispatch_mxfp4(const void *tokens, int64_t token_stride, int64_t num_tokens,
                                 int64_t hidden, const int32_t *topk_ids, int32_t top_k,
                                 int32_t num_experts, uint8_t *out, uint8_t *scales,
                                 int64_t scale_rows_total, uint32_t *row_offsets,
-                                int32_t *expert_ids, int32_t *src_info,
+                                int32_t *expert_ids, int32_t *src_info, int32_t *dst_info,
                                 uint32_t *scales_offsets, int32_t slot_rows,
                                 moeq_stream_t stream);
 

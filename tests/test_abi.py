@@ -84,35 +84,59 @@ def test_layout_helpers_reject_bad_host_arguments(lib):
 
 def test_route_and_dispatch_reject_bad_host_arguments(lib):
     r = lib.moeq_route_topk
-    #        ids   T   k  E    ro    eids  src   so    slot stream
-    assert r(FAKE, 8, 0, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # top_k < 1
-    assert r(FAKE, 8, 2, 0, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # no experts
-    assert r(FAKE, 8, 2, 2000, FAKE, FAKE, FAKE, FAKE, 0, None) == 2   # above 1024 experts
-    assert r(FAKE, 8, 2, 4, FAKE, FAKE, FAKE, FAKE, 100, None) == 1    # slot % 128
-    assert r(FAKE, 8, 2, 4, None, FAKE, FAKE, FAKE, 0, None) == 1      # row_offsets
-    assert r(None, 8, 2, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 1      # topk_ids with tokens
-    assert r(FAKE, 8, 2, 4, FAKE, FAKE, ODD, FAKE, 0, None) == 1       # misaligned
-    assert r(FAKE, 1 << 30, 4, 4, FAKE, FAKE, FAKE, FAKE, 0, None) == 2   # 2^32 choices
+
+    def route(ids=FAKE, T=8, k=2, E=4, ro=FAKE, eids=FAKE, src=FAKE, dst=None, so=FAKE, slot=0):
+        return r(ids, T, k, E, ro, eids, src, dst, so, slot, None)
+
+    assert route(k=0) == 1                  # top_k < 1
+    assert route(E=0) == 1                  # no experts
+    assert route(E=2000) == 2               # above 1024 experts
+    assert route(slot=100) == 1             # slot % 128
+    assert route(ro=None) == 1              # row_offsets
+    assert route(ids=None) == 1             # topk_ids with tokens
+    assert route(src=ODD) == 1              # misaligned
+    assert route(dst=ODD) == 1
+    assert route(T=1 << 30, k=4) == 2       # 2^32 choices
     rows = lib.moeq_dispatch_scale_rows
+    rows.restype = ctypes.c_int64
     assert rows(100, 8, 16, 0) == (800 + 127 * 16) // 128 * 128
     assert rows(100, 8, 16, 256) == 16 * 256
     assert rows(-1, 8, 16, 0) == -1
     d = lib.moeq_dispatch_mxfp4
     ok = dict(tok=FAKE, stride=256, T=8, H=256, ids=FAKE, k=2, E=4, out=FAKE, sf=FAKE,
-              srows=rows(8, 2, 4, 0), ro=FAKE, eids=FAKE, src=FAKE, so=FAKE, slot=0, s=None)
+              srows=rows(8, 2, 4, 0), ro=FAKE, eids=FAKE, src=FAKE, dst=FAKE, so=FAKE, slot=0,
+              s=None)
 
     def call(**kw):
         a = dict(ok, **kw)
         return d(a["tok"], a["stride"], a["T"], a["H"], a["ids"], a["k"], a["E"], a["out"],
-                 a["sf"], a["srows"], a["ro"], a["eids"], a["src"], a["so"], a["slot"], a["s"])
+                 a["sf"], a["srows"], a["ro"], a["eids"], a["src"], a["dst"], a["so"], a["slot"],
+                 a["s"])
 
     assert call(H=200) == 1                 # hidden % 128
     assert call(stride=128) == 1            # stride < hidden
     assert call(srows=0) == 1               # no scale rows
     assert call(srows=ok["srows"] - 128) == 1   # fewer scale rows than needed
     assert call(so=None) == 1               # scale offsets required
+    assert call(dst=None) == 1              # the inverse map is required
     assert call(out=ODD) == 1
     assert call(slot=128, srows=4 * 128 - 128) == 1
+    assert call(k=9, srows=rows(8, 9, 4, 0)) == 2   # token-major quantization: top_k <= 8
+    q = lib.moeq_quantize_topk
+    okq = dict(fmt=0, tok=FAKE, stride=256, T=8, K=256, ids=FAKE, k=2, dst=FAKE, ro=FAKE,
+               so=FAKE, ts=FAKE, E=4, out=FAKE, sf=FAKE, srows=512, s=None)
+
+    def callq(**kw):
+        a = dict(okq, **kw)
+        return q(a["fmt"], a["tok"], a["stride"], a["T"], a["K"], a["ids"], a["k"], a["dst"],
+                 a["ro"], a["so"], a["ts"], a["E"], a["out"], a["sf"], a["srows"], a["s"])
+
+    assert callq(fmt=5) == 1
+    assert callq(K=100) == 1                # K % 128
+    assert callq(ts=None) == 1              # NVFP4 needs the tensor scales
+    assert callq(dst=None) == 1
+    assert callq(srows=100) == 1
+    assert callq(k=9) == 2                  # top_k <= 8
 
 
 def test_gemms_reject_bad_host_arguments(lib):

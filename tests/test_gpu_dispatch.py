@@ -294,3 +294,50 @@ def test_topk_amax_skips_invalid_ids():
     assert np.array_equal(ts.cpu().numpy().view(np.uint32), ref.view(np.uint32))
     assert moeq.get_device_error() & moeq.DEVERR_BAD_EXPERT
     moeq.clear_device_error()
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "mxfp8"])
+@pytest.mark.parametrize("T,K,E,k,slot_rows", [(600, 1024, 8, 4, 0), (600, 640, 8, 4, 768),
+                                               (333, 512, 16, 8, 0), (16384, 4096, 128, 8, 0)])
+def test_quantize_topk_equals_the_gathered_quantizer(fmt, T, K, E, k, slot_rows):
+    """Token-major quantization (each token read once, written to its routed
+    rows) gives the whole output and scale buffers of the gathered quantizer
+    byte for byte, canary bytes included; a few choices are dropped."""
+    need_gpu()
+    moeq.clear_device_error()
+    tok = synth.bf16_normal((T, K), 1.0, seed=101 + T, device=DEV, outlier_p=0.003,
+                            outlier_scale=40.0)
+    ids = _topk(T, k, E, seed=102, zipf=0.9)
+    if T < 1000:
+        ids[7, 1] = -1
+        ids[T - 1, 0] = E
+    tk = torch.from_numpy(ids).to(DEV)
+    n = T * k
+    i32 = dict(dtype=torch.int32, device=DEV)
+    ro, eids, src, dst, so = (torch.empty(E + 1, **i32), torch.empty(E, **i32),
+                              torch.empty(n, **i32), torch.empty(n, **i32),
+                              torch.empty(E + 1, **i32))
+    moeq.route_topk(tk, ro, eids, src, so, slot_rows, dst_info=dst)
+    ts = torch.empty(E, device=DEV)
+    moeq.grouped_amax_scale_topk(tok, tk, ts, E)
+    rows = moeq.dispatch_scale_rows(T, k, E, slot_rows)
+    ob = K if fmt == "mxfp8" else K // 2
+    v = 16 if fmt == "nvfp4" else 32
+    outs = []
+    for token_major in (True, False):
+        out = torch.full((n, ob), 0xA5, dtype=torch.uint8, device=DEV)
+        sf = torch.full((moeq.sf_bytes(rows, K // v),), 0x5A, dtype=torch.uint8, device=DEV)
+        if token_major:
+            moeq.quantize_topk(fmt, tok, tk, dst, out, sf, ro, so, ts, E)
+        else:
+            moeq.grouped_quantize_gather(fmt, tok, src, k, out, sf, ro, so, eids, ts, E, rows)
+        outs.append((out, sf))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    routed = int(ro[-1])
+    assert (outs[0][0][:routed] != 0xA5).float().mean() > 0.5
+    bits = moeq.get_device_error()
+    assert (bits & ~moeq.DEVERR_BAD_EXPERT) == 0
+    moeq.clear_device_error()
+    note(choices=n, routed=routed)
