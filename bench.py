@@ -671,6 +671,12 @@ def run_e2e(d, args, world, fl, form):
                      "131072 pre-gathered bf16 rows x 4096 + group offsets"),
            "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
            "single_copy_h2d_GB/s": round(big / h0.elapsed_time(h1) / 1e6, 1)}
+    # the same compute without the copies, device time (CUDA events)
+    dev_ms = time_kernel(lambda: compute(bufs[0]), steps)
+    out["device_step_ms"] = round(dev_ms, 4)
+    out["device_step_note"] = ("the compute of one step alone, inputs resident; the row-level "
+                               "step of `value` quantizes through the group lookup, the token "
+                               "form reads each token once")
     del bufs
     return out
 
