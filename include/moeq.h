@@ -29,6 +29,11 @@
  *   expert, each ceil(N / 128) * ceil(Kv / 4) * 512 bytes.
  * - FP4 elements are packed two per byte, the lower-k element in the low
  *   nibble.
+ * - Routed tokens ("Struct_ep_dispatch_mxfp4", execute, on one rank):
+ *   moeq_route_topk turns per-token top-k expert ids into the group layout
+ *   above (group e = expert e, every expert, stable order);
+ *   moeq_grouped_amax_scale_topk and moeq_quantize_topk then read each token
+ *   once and give the bytes of the row-level calls on the routed rows.
  * - num_active_experts == 0 (or zero total rows) is MOEQ_OK and launches
  *   nothing.  max_tokens_per_expert is a sizing hint ("Max tokens routed to
  *   any active expert"): it picks launch shapes only, and groups larger than
