@@ -490,6 +490,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // Cluster-wide barrier: every thread of every CTA of the cluster arrives.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"

@@ -4,7 +4,8 @@
 // all-to-all exchange is the identity).  Group e is expert e (empty groups
 // kept); a group's rows hold its choices i = t * top_k + k in increasing i.
 //
-// One cluster of kRouteCtas CTAs of 32 warps and no memory besides the
+// One cluster of 16 CTAs (8, the portable size, where 16 cannot be
+// resident) of 32 warps and no memory besides the
 // caller's outputs.  CTA c owns a contiguous chunk of the choices and warp
 // w of it a contiguous segment of that chunk.  Pass 1 builds one histogram
 // per warp in shared memory; each CTA turns them into per-warp prefixes and
@@ -25,7 +26,8 @@ namespace moeq {
 
 namespace {
 
-constexpr int kRouteCtas = 8;                // portable cluster size
+constexpr int kRouteCtasMax = 16;  // non-portable cluster size, when it fits
+constexpr int kRouteCtasPortable = 8;
 constexpr int kRouteWarps = 32;
 constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kRouteU = 16;  // 32-choice batches whose loads a warp issues together
@@ -78,6 +80,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t rank = cluster_ctarank();
+    const int nct = (int)cluster_nctarank();
     uint32_t *cnt = hist + kRouteWarps * E;
     uint32_t *tot = cnt + E;
     uint32_t *before_chunk = tot + E;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     __syncthreads();
 
     // pass 1: per-warp histograms over contiguous segments of this chunk
-    const int64_t per_cta = (n + kRouteCtas - 1) / kRouteCtas;
+    const int64_t per_cta = (n + nct - 1) / nct;
     const int64_t c0 = min(n, (int64_t)rank * per_cta), c1 = min(n, c0 + per_cta);
     const int64_t per = (c1 - c0 + kRouteWarps - 1) / kRouteWarps;
     const int64_t s0 = min(c1, c0 + (int64_t)warp * per), s1 = min(c1, s0 + per);
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     uint32_t rows = 0, pad = 0;
     for (int e = e0; e < e1; ++e) {
         uint32_t t = 0, before = 0;
-        for (int c = 0; c < kRouteCtas; ++c) {
+        for (int c = 0; c < nct; ++c) {
             const uint32_t v = ld_cluster_u32(mapa_shared(cnt_addr + 4u * e, (uint32_t)c));
             if (c < (int)rank) before += v;
             t += v;
@@ -220,16 +223,37 @@ cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kRouteCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = kPdl;
-    cfg.gridDim = dim3(kRouteCtas, 1, 1);
     cfg.blockDim = dim3(kRouteThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
+    // per device and shared-memory size: the cluster size that can be
+    // resident (16 when the non-portable size fits, else 8)
+    static int ctas_for[64] = {0};
+    static size_t ctas_smem[64] = {0};
+    if (!ctas_for[dev] || ctas_smem[dev] != smem) {
+        int ctas = kRouteCtasPortable;
+        if (cudaFuncSetAttribute(route_topk_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+            attr[0].val.clusterDim.x = kRouteCtasMax;
+            cfg.gridDim = dim3(kRouteCtasMax, 1, 1);
+            cfg.numAttrs = 1;
+            int active = 0;
+            if (cudaOccupancyMaxActiveClusters(&active, route_topk_kernel, &cfg) == cudaSuccess &&
+                active >= 1)
+                ctas = kRouteCtasMax;
+        }
+        cudaGetLastError();  // a refused query is not a launch error
+        ctas_for[dev] = ctas;
+        ctas_smem[dev] = smem;
+    }
+    attr[0].val.clusterDim.x = ctas_for[dev];
+    cfg.gridDim = dim3(ctas_for[dev], 1, 1);
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, route_topk_kernel, topk_ids, num_choices, num_experts,
                               row_offsets, expert_ids, src_info, dst_info, scales_offsets,
