@@ -3,7 +3,7 @@
 // epilogue or the fused SwiGLU + NVFP4 requantization epilogue.
 //
 // Pages: "grouped_matmul_rowwise_dynamic_scaled_fp8" (the rowwise formula,
-// fp32 accumulation, one post-reduction scale; its documented kernel is a
+// fp32 accumulation, scaled once after the reduction; its documented kernel is a
 // naive one with no persistent or TMA path), "max.nn.moe.NvMxf4f8Strategy"
 // (grouped_matmul: block-scaled with per-expert scales; grouped_matmul_swiglu:
 // GEMM + SwiGLU + quantize in one kernel, byte-identical to the chained path).

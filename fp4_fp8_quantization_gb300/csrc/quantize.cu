@@ -9,7 +9,8 @@
 // Pages: "grouped_quantize_dynamic_scaled_fp4_async_kernel" (each block finds
 // its expert by binary search on row_offsets / scales_offsets, then
 // quantizes that expert's BF16 rows); "max.nn.moe.NvMxf4f8Strategy"
-// (grouped_quantize with padded scale alignment; fused_silu_quantize).
+// (grouped_quantize: per-expert quantization with padded scales;
+// fused_silu_quantize).
 #include "common.cuh"
 #include "launch.h"
 

@@ -16,7 +16,7 @@
  *   int32 [G].  Empty groups write nothing.  Rows outside every group are
  *   never written.
  * - Padded scale rows ("max.nn.moe.NvMxf4f8Strategy", grouped_quantize:
- *   "padded scale alignment"; "grouped_quantize_dynamic_scaled_fp4_async_kernel",
+ *   per-expert padding of the scales; "grouped_quantize_dynamic_scaled_fp4_async_kernel",
  *   scales_offsets): the block scales of group g live in logical scale rows
  *   [scales_offsets[g], scales_offsets[g+1]); scales_offsets[g] must be a
  *   multiple of 128 and leave room for ceil(r_g / 128) * 128 rows.
@@ -35,8 +35,8 @@
  *   moeq_grouped_amax_scale_topk and moeq_quantize_topk then read each token
  *   once and give the bytes of the row-level calls on the routed rows.
  * - num_active_experts == 0 (or zero total rows) is MOEQ_OK and launches
- *   nothing.  max_tokens_per_expert is a sizing hint ("Max tokens routed to
- *   any active expert"): it picks launch shapes only, and groups larger than
+ *   nothing.  max_tokens_per_expert is a sizing hint (the largest token
+ *   count of any active expert): it picks launch shapes only, and groups larger than
  *   it are still computed in full.
  * - Errors.  Bad host arguments return MOEQ_ERR_INVALID_ARG before anything
  *   is launched (this includes a missing NVFP4 scale tensor, the pages'
@@ -182,7 +182,7 @@ moeq_status moeq_padded_scale_offsets(const uint32_t *row_offsets,
  * the reduction (acc * a_scale first, then * b_scale), round to nearest even.
  *   c         bf16 [total_tokens, N]
  *   a         E4M3 [total_tokens, K]
- *   b         E4M3 [num_experts, N, K] (K innermost; "transpose_b must be True")
+ *   b         E4M3 [num_experts, N, K] (K innermost: the page accepts only transposed b)
  *   a_scales  fp32 [total_tokens];  b_scales fp32 [num_experts, N]
  * K % 128 == 0, N % 16 == 0. */
 moeq_status moeq_grouped_matmul_rowwise_fp8(
@@ -193,9 +193,8 @@ moeq_status moeq_grouped_matmul_rowwise_fp8(
     int32_t num_active_experts, moeq_stream_t stream);
 
 /* Grouped block-scaled matmul with per-expert epilogue scales
- * ("max.nn.moe.NvMxf4f8Strategy", grouped_matmul: "grouped NVIDIA
- * block-scaled matmul with per-expert scales"; expert_scales are the
- * "per-expert matmul-epilogue scaling factors"):
+ * ("max.nn.moe.NvMxf4f8Strategy", grouped_matmul: a grouped block-scaled
+ * matmul with one scale per expert, applied in the matmul epilogue):
  *   c[t, n] = bf16( expert_scales[e] * sum_k (qa[t,k] * sa[t,k/v]) * (qb[e,n,k] * sb[e,n,k/v]) )
  * with e = expert_ids[g], v = 16 (NVFP4) or 32 (MXFP8, MXFP4).
  *   a      NVFP4 / MXFP4: packed [total_tokens, K/2]; MXFP8: [total_tokens, K]
@@ -214,7 +213,7 @@ moeq_status moeq_grouped_matmul_blockscaled(
     int32_t num_active_experts, moeq_stream_t stream);
 
 /* Chained SwiGLU + NVFP4 requantization ("max.nn.moe.NvMxf4f8Strategy",
- * fused_silu_quantize: applies the gated activation then quantizes; the
+ * fused_silu_quantize: the gated activation, then quantization; the
  * SiLU-output scale is passed raw and inverted inside, as
  * prepare_swiglu_operands requires).
  *   y      bf16 [total_tokens, 2I]: column 2j = gate_j, 2j+1 = up_j
@@ -269,8 +268,8 @@ moeq_status moeq_swiglu_quantize_mx(moeq_format fmt, uint8_t *c_q, uint8_t *c_sf
  * interleaved (row 2j = gate_j, row 2j+1 = up_j); b_sf its per-expert tiled
  * scales.  expert_scales and out_tensor_scale are required.
  *   a_row_scales  optional bf16 [total_tokens] (NULL = none; grouped_matmul_swiglu:
- *            "BF16 scale per hidden row, applied with the expert scale
- *            before the SwiGLU"): gate and up become
+ *            one bf16 scale per row, applied with the expert scale ahead
+ *            of the SwiGLU): gate and up become
  *            bf16((acc * expert_scale) * a_row_scale[t]), two fp32 multiplies
  *            in that order.  With row scales there is no chained counterpart.
  * K % 256 == 0, I % 64 == 0. */
@@ -301,7 +300,7 @@ moeq_status moeq_grouped_matmul_swiglu_mx(
     moeq_stream_t stream);
 
 /* ---- weight preparation ("max.nn.moe.NvMxf4f8Strategy", prepare_weight_scales:
- * "interleaves NVIDIA block scales for kernel layout").  Run once per weight,
+ * block scales rearranged into the kernel's layout).  Run once per weight,
  * off the per-step path.  Every pointer is a caller-owned device pointer;
  * the calls only enqueue work on `stream`.  batch, rows, kv / row_bytes == 0
  * is MOEQ_OK and a no-op; negative sizes or NULL pointers (with a non-empty

@@ -1,9 +1,9 @@
 """Block-scale memory layout (the index function), TEST INFRASTRUCTURE ONLY.
 
 The pages give no layout: "max.nn.moe.NvMxf4f8Strategy" says only that the
-activation scales are padded per expert (``grouped_quantize``: "padded
-scale alignment") and that ``prepare_weight_scales`` "interleaves NVIDIA
-block scales for kernel layout"; "grouped_quantize_dynamic_scaled_fp4_async_kernel"
+activation scales are padded per expert (``grouped_quantize``) and that
+``prepare_weight_scales`` rearranges the weight block scales into the
+kernel's layout; "grouped_quantize_dynamic_scaled_fp4_async_kernel"
 stores them through a TMA tile descriptor.  Reading adopted: the canonical
 layout is the tensor core's tiled scale layout --
 

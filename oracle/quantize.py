@@ -9,7 +9,7 @@ Sources.
   scale factors; ``sf_tensor`` is a read-only per-expert fp32 tensor-wise
   scale.
 * "max.nn.moe.NvMxf4f8Strategy", ``grouped_quantize``: per-expert
-  quantization "with padded scale alignment".
+  quantization with the scales padded per expert.
 * The pages fix no formula.  The readings used here (stated once, used by
   the oracle and the kernels alike):
   - NVFP4: 16-element blocks, E2M1 elements, E4M3 block scale, per-expert
