@@ -81,9 +81,9 @@ def grouped_matmul_blockscaled(fmt, a, a_sf, b, b_sf, expert_scales, a_offsets,
     buffer of [scale_rows_total, K/v]; b: [E, N, K/2] or [E, N, K]; b_sf:
     per-expert tiled buffers.  Row t of group g uses scale row
     a_scales_offsets[g] + (t - a_offsets[g]).  row_scales (optional, [T]
-    values of bf16 numbers): the per-row scale of grouped_matmul_swiglu
-    ("applied with the expert scale"), multiplied in with the expert scale
-    before the single rounding to bf16."""
+    values of bf16 numbers): the per-row scale of grouped_matmul_swiglu,
+    which the page applies together with the expert scale; multiplied in
+    with the expert scale before the single rounding to bf16."""
     v = 16 if fmt == "nvfp4" else 32
     kv = K // v
     a = np.asarray(a, np.uint8)
