@@ -217,9 +217,17 @@ moeq_status moeq_grouped_matmul_blockscaled(
  * SiLU-output scale is passed raw and inverted inside, as
  * prepare_swiglu_operands requires).
  *   y      bf16 [total_tokens, 2I]: column 2j = gate_j, 2j+1 = up_j
- *   h_j    = silu(gate_j) * up_j in fp32, silu(g) = g / (1 + exp(-g)) with the
- *            library's own deterministic fp32 exp (Cody-Waite reduction,
- *            degree-7 Taylor polynomial, no fused multiply-add)
+ *   h_j    = silu(gate_j) * up_j in fp32, silu(g) = g * sigma(g) with the
+ *            library's own deterministic sigma, each step one IEEE fp32
+ *            operation or one fused multiply-add:
+ *              e = exp(-|g|): Cody-Waite reduction (ln 2 split into a
+ *                  16-bit head and an fp32 tail, n from one FMA with the
+ *                  1.5 * 2^23 shift), degree-7 Taylor polynomial by Horner
+ *                  in FMAs, times 2^n (2^n taken as 0 for n < -126);
+ *              d = 1 + e;  r = 1 / d by three Newton steps in FMAs
+ *                  (q = 1 - d r, r = r + r q) from 24/17 - 8/17 d;
+ *              sigma = r for g >= 0, e * r otherwise.
+ *            CUDA's expf and IEEE division are not used.
  *   c_packed  NVFP4 [total_tokens, I/2];  c_sf tiled scales [scale_rows_total
  *            rows x I/16], padded per expert exactly like moeq_grouped_quantize
  *   out_tensor_scale  fp32 [num_experts] raw s_e (required).
