@@ -13,17 +13,17 @@ __device__ uint32_t g_device_error;
 
 thread_local int t_last_cuda_error = 0;
 
-// Address of the device error word on the current device (cached).
+// Address of the device error word on the current device (looked up once
+// per device).
 uint32_t *device_error_ptr() {
-    static uint32_t *cache[64] = {nullptr};
+    static std::atomic<uint32_t *> cache[moeq::kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= moeq::kMaxDevices) return nullptr;
+    return moeq::cached_per_device(cache, dev, []() -> uint32_t * {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<uint32_t *>(p);
-    }
-    return cache[dev];
+        return static_cast<uint32_t *>(p);
+    });
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -57,6 +57,11 @@ moeq::GroupArgs make_groups(const uint32_t *ro, const uint32_t *so, const int32_
 }
 
 }  // namespace
+
+std::mutex &moeq::launch_setup_mutex() {
+    static std::mutex m;
+    return m;
+}
 
 extern "C" {
 

@@ -806,15 +806,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe static initialisation)
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -868,16 +869,15 @@ bool make_sfb_map(CUtensorMap *m, const void *base, int64_t row_blocks, int64_t 
 }
 
 int sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cache[dev]) {
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    return cached_per_device(cache, dev, [dev]() {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 1;
-    }
-    return cache[dev];
+        return n > 0 ? n : 1;
+    });
 }
 
 template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1,
@@ -931,20 +931,20 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     const int64_t tiles_ub = (T / (C::BM * PAIR) + a.groups.num_groups) * nb;
     auto kern = grouped_gemm_kernel<C, KIND, EPI>;
     // per-device launch set-up of this kernel, done once (the shared-memory
-    // attribute and, for pairs, the resident cluster count); concurrent
-    // first calls only repeat the same idempotent queries
-    static int attr_done[64] = {0};
-    static int max_cl_cache[64] = {0};
+    // attribute and, for pairs, the resident cluster count)
+    static std::atomic<int> attr_done[kMaxDevices];
+    static std::atomic<int> max_cl_cache[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = 1;
-    }
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaError_t attr_err = cudaSuccess;
+    cached_per_device(attr_done, dev, [&]() {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::SMEM_BYTES);
+        return attr_err == cudaSuccess ? 1 : 0;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     if (PAIR == 1) {
         const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
         return launch_pdl(kern, grid, C::THREADS, C::SMEM_BYTES, s, tA, tB, tSFA, tSFB, p);
@@ -964,13 +964,14 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(sm_count() / PAIR * PAIR), 1, 1);
-    int max_clusters = max_cl_cache[dev];
-    if (!max_clusters) {
-        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (max_clusters < 1) return cudaErrorNotSupported;
-        max_cl_cache[dev] = max_clusters;
-    }
+    cudaError_t occ_err = cudaSuccess;
+    const int max_clusters = cached_per_device(max_cl_cache, dev, [&]() {
+        int n = 0;
+        occ_err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        return occ_err == cudaSuccess && n >= 1 ? n : 0;
+    });
+    if (occ_err != cudaSuccess) return occ_err;
+    if (max_clusters < 1) return cudaErrorNotSupported;
     int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * PAIR), 1, 1);
     cfg.numAttrs = 2;

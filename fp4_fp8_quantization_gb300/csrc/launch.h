@@ -6,7 +6,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace moeq {
+
+// Per-device launch set-up (SM counts, kernel attributes already applied,
+// occupancy answers) is computed once per device and cached.  The library
+// may be called from several host threads at once, so every cache entry is
+// an atomic, read without a lock and filled under launch_setup_mutex().
+constexpr int kMaxDevices = 64;
+std::mutex &launch_setup_mutex();
+
+// cache[dev], filled once by fill() (a non-zero value; 0 means the set-up
+// failed and leaves the entry empty, so a later call retries).
+template <class T, class F>
+T cached_per_device(std::atomic<T> (&cache)[kMaxDevices], int dev, F fill) {
+    T v = cache[dev].load(std::memory_order_acquire);
+    if (v) return v;
+    std::lock_guard<std::mutex> lock(launch_setup_mutex());
+    v = cache[dev].load(std::memory_order_relaxed);
+    if (!v) {
+        v = fill();
+        if (v) cache[dev].store(v, std::memory_order_release);
+    }
+    return v;
+}
 
 struct GroupArgs {
     const uint32_t *row_offsets;     // [G+1]

@@ -74,16 +74,15 @@ __global__ void interleave_rows_kernel(T *__restrict__ out, const T *__restrict_
 }
 
 int sm_count_cached() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cache[dev]) {
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    return cached_per_device(cache, dev, [dev]() {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 1;
-    }
-    return cache[dev];
+        return n > 0 ? n : 1;
+    });
 }
 
 // grid-stride launches: up to 16 blocks of 256 threads per SM

@@ -208,12 +208,15 @@ cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int 
                               int32_t *dst_info, uint32_t *scales_offsets, int slot_rows,
                               uint32_t *err, cudaStream_t s) {
     const size_t smem = route_smem_bytes(num_experts);
-    // per device, the largest dynamic shared memory set so far
-    static size_t smem_set[64] = {0};
+    // per device, the largest dynamic shared memory set so far and the
+    // cluster size for the last shared-memory size queried; the set-up runs
+    // under the library's launch lock (concurrent host threads)
+    static size_t smem_set[kMaxDevices] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::unique_lock<std::mutex> lock(launch_setup_mutex());
     if (smem > 48 * 1024 && smem > smem_set[dev]) {
         e = cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
@@ -233,8 +236,8 @@ cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int 
     cfg.attrs = attr;
     // per device and shared-memory size: the cluster size that can be
     // resident (16 when the non-portable size fits, else 8)
-    static int ctas_for[64] = {0};
-    static size_t ctas_smem[64] = {0};
+    static int ctas_for[kMaxDevices] = {0};
+    static size_t ctas_smem[kMaxDevices] = {0};
     if (!ctas_for[dev] || ctas_smem[dev] != smem) {
         int ctas = kRouteCtasPortable;
         if (cudaFuncSetAttribute(route_topk_kernel,
@@ -252,8 +255,10 @@ cudaError_t launch_route_topk(const int32_t *topk_ids, int64_t num_choices, int 
         ctas_for[dev] = ctas;
         ctas_smem[dev] = smem;
     }
-    attr[0].val.clusterDim.x = ctas_for[dev];
-    cfg.gridDim = dim3(ctas_for[dev], 1, 1);
+    const int ctas = ctas_for[dev];
+    lock.unlock();
+    attr[0].val.clusterDim.x = ctas;
+    cfg.gridDim = dim3(ctas, 1, 1);
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, route_topk_kernel, topk_ids, num_choices, num_experts,
                               row_offsets, expert_ids, src_info, dst_info, scales_offsets,

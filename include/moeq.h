@@ -34,6 +34,12 @@
  *   above (group e = expert e, every expert, stable order);
  *   moeq_grouped_amax_scale_topk and moeq_quantize_topk then read each token
  *   once and give the bytes of the row-level calls on the routed rows.
+ * - Host threads.  Calls may be made concurrently from several host threads,
+ *   on the same or different streams.  The only host state the library
+ *   keeps is per-device launch set-up (SM count, kernel attributes applied,
+ *   occupancy answers), computed once per device under an internal lock.
+ *   moeq_last_cuda_error() is per host thread.  The device error word is
+ *   shared by every call on a device.
  * - num_active_experts == 0 (or zero total rows) is MOEQ_OK and launches
  *   nothing.  max_tokens_per_expert is a sizing hint (the largest token
  *   count of any active expert): it picks launch shapes only, and groups larger than
