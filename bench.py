@@ -22,6 +22,7 @@ its own batch (weak scaling, no collective on the data path); the time is the
 maximum over ranks.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -42,10 +43,46 @@ WORKLOAD = ("NVFP4 MoE up-projection: 128 experts, 16384 tokens top-8 uniform ->
 E4, TOK4, TOPK4, K4, I4 = 128, 16384, 8, 4096, 1536
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratios
 FP8_OVER_BF16 = 4.5 / 2.25
-# DRAM bytes (read + write) of one launch of the fused GEMM on this workload,
-# from one ncu capture of the current kernel (1.211 GB read + 110.7 MB
-# written); None until the current kernel has been captured.
-FUSED_TRAFFIC_BYTES = 1.3218e9
+# nominal figures of the part (dense tensor rates, HBM3e bandwidth)
+NOMINAL = {"hbm_gbs": 7900.0, "fp8_tflops": 4500.0, "fp4_tflops": 13500.0}
+# Measured tcgen05 MMA ceiling of this part: one M128 x N256 instruction per
+# 128 SM cycles for every kind, so FP4 (K = 64) does 2 * 128 * 256 * 64 / 128
+# = 32768 flop per SM cycle (FP8 half, bf16 a quarter).
+FP4_FLOP_PER_SM_CYCLE = 32768
+# The fused GEMM's DRAM traffic comes from a committed ncu summary that names
+# the sha256 of the kernel sources it was captured with; a changed kernel
+# makes the figure stale and the bench reports null.
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "launches_moe_up_projection_nvfp4_128experts.md")
+KERNEL_SOURCES = ("fp4_fp8_quantization_gb300/csrc/gemm.cu",
+                  "fp4_fp8_quantization_gb300/csrc/common.cuh")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def fused_traffic_bytes():
+    """(bytes per launch, note): the DRAM read + write bytes of one full-size
+    fused launch from the committed ncu summary, or None when the summary was
+    captured with other kernel sources (or is missing)."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None, "no ncu summary"
+    src = traf = None
+    for line in text.splitlines():
+        if line.startswith("kernel-sources-sha256:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("fused-gemm-dram-bytes-per-launch:"):
+            traf = float(line.split(":", 1)[1].strip())
+    cur = kernel_source_hash()
+    if traf is None or src != cur:
+        return None, f"ncu summary captured with kernel sources {src}, current {cur}: not re-captured"
+    return traf, f"ncu dram__bytes_read.sum + dram__bytes_write.sum, kernel sources {cur}"
 
 
 def emit(line, args):
@@ -165,24 +202,66 @@ class Clocks:
 
 # --------------------------------------------------------------- workload
 
+def nvfp4_expert_weights(num_experts, rows, K, std, seed, device="cuda"):
+    """(packed [E, rows, K/2], tiled scales, tensor scales [E]): expert
+    weights drawn as bf16 N(0, std) and quantized to NVFP4 by the library's
+    own grouped quantizer, one group per expert (each expert's tensor scale
+    from its amax)."""
+    from fp4_fp8_quantization_gb300 import moeq, synth
+    w = synth.bf16_normal((num_experts * rows, K), std, seed=seed, device=device)
+    offs = torch.arange(num_experts + 1, dtype=torch.int32, device=device) * rows
+    ids = torch.arange(num_experts, dtype=torch.int32, device=device)
+    ts = torch.empty(num_experts, device=device)
+    moeq.grouped_amax_scale(w, offs, ids, ts, num_experts)
+    b = torch.empty((num_experts * rows, K // 2), dtype=torch.uint8, device=device)
+    bsf = torch.empty(moeq.sf_bytes(num_experts * rows, K // 16), dtype=torch.uint8,
+                      device=device)
+    moeq.grouped_quantize("nvfp4", w, b, bsf, offs, offs, ids, ts, num_experts,
+                          num_experts * rows, rows)
+    del w
+    return b.view(num_experts, rows, K // 2), bsf, ts
+
+
+def swiglu_output_scales(y, ro, ids, num_experts):
+    """Calibration of the SwiGLU output's NVFP4 tensor scale on the chained
+    path's bf16 y: amax over each expert group of silu(gate) * up in fp32,
+    / 2688 (1 for an empty or all-zero group).  PyTorch's fp32 SiLU stands in
+    for the library's here: the result is an input scale, valid at any
+    positive value."""
+    out = torch.ones(num_experts, dtype=torch.float32, device=y.device)
+    for g in range(len(ids)):
+        r0, r1 = int(ro[g]), int(ro[g + 1])
+        if r1 == r0:
+            continue
+        yy = y[r0:r1].float()
+        h = torch.nn.functional.silu(yy[:, 0::2]) * yy[:, 1::2]
+        amax = float(h.abs().max())
+        if amax > 0:
+            out[int(ids[g])] = float(np.float32(amax) / np.float32(2688.0))
+    return out
+
+
 def up_projection_inputs(seed, device="cuda"):
+    """The 128-expert up-projection as configured: activations bf16 N(0, 1)
+    (quantized in the timed step), gate/up weights NVFP4 from bf16 N(0, 0.02)
+    with per-expert tensor scales, expert scales U[0.5, 2], and the SwiGLU
+    output scales from a calibration run of the chained path on these
+    inputs."""
     from fp4_fp8_quantization_gb300 import moeq, synth
     counts = synth.routing_counts(TOK4, TOPK4, E4, seed=seed)
     ro, ids = synth.ragged_groups(counts)
     T = int(ro[-1])
     rows = int(sum((int(c) + 127) // 128 * 128 for c in counts if c))
     N = 2 * I4
+    b, bsf, ts_w = nvfp4_expert_weights(E4, N, K4, 0.02, seed + 2, device)
     d = {
         "counts": counts, "ro_h": ro, "ids_h": ids, "T": T, "rows": rows, "N": N,
         "ro": torch.from_numpy(ro.view(np.int32)).to(device),
         "ids": torch.from_numpy(ids).to(device),
         "so": torch.empty(len(ids) + 1, dtype=torch.int32, device=device),
         "x": synth.bf16_normal((T, K4), 1.0, seed=seed + 1, device=device),
-        "b": synth.random_fp4_packed((E4, N, K4 // 2), seed=seed + 2, device=device),
-        "bsf": synth.random_bytes(E4 * moeq.sf_bytes(N, K4 // 16), 0x18, 0x28, seed=seed + 3,
-                                  device=device),
+        "b": b, "bsf": bsf, "ts_w": ts_w,
         "es": synth.uniform((E4,), 0.5, 2.0, seed=seed + 4, device=device),
-        "ots": synth.uniform((E4,), 1.0, 4.0, seed=seed + 5, device=device),
         "ts": torch.empty(E4, device=device),
         "a": torch.empty((T, K4 // 2), dtype=torch.uint8, device=device),
         "asf": torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8, device=device),
@@ -190,6 +269,16 @@ def up_projection_inputs(seed, device="cuda"):
         "csf": torch.empty(moeq.sf_bytes(rows, I4 // 16), dtype=torch.uint8, device=device),
     }
     d["mt"] = int(counts.max())
+    # calibration: quantize the activations, chained GEMM -> bf16 y, amax of h
+    moeq.padded_scale_offsets(d["ro"], d["so"])
+    moeq.grouped_amax_scale(d["x"], d["ro"], d["ids"], d["ts"], E4)
+    moeq.grouped_quantize("nvfp4", d["x"], d["a"], d["asf"], d["ro"], d["so"], d["ids"], d["ts"],
+                          E4, rows, d["mt"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=device)
+    moeq.grouped_matmul_blockscaled("nvfp4", y, d["a"], d["asf"], b, bsf, d["es"], d["ro"],
+                                    d["so"], d["ids"], N, K4, rows, d["mt"])
+    d["ots"] = swiglu_output_scales(y, ro, ids, E4)
+    del y
     return d
 
 
@@ -283,7 +372,8 @@ def parts(pk, flush):
         nbytes = T * 4096 * 2 + qs[0].numel() + sfs[0].numel()
         out[f"quantize_{fmt}_8192x4096"] = {
             "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
-            "frac_hbm": round(nbytes / ms / 1e6 / hbm, 4), "bytes": nbytes,
+            "frac_hbm": round(nbytes / ms / 1e6 / hbm, 4),
+            "frac_hbm_nominal": round(nbytes / ms / 1e6 / NOMINAL["hbm_gbs"], 4), "bytes": nbytes,
             "l2": "4 rotating input sets (268 MB > L2)",
             "timing": "median over 20 batches of 8 back-to-back calls"}
     out["amax_8192x4096"] = {"ms": round(t_amax, 5),
@@ -301,10 +391,29 @@ def parts(pk, flush):
     sb_t = synth.uniform((4, 64), 0.005, 0.05, seed=43, device=dev)
     c_t = torch.empty((32, 64), dtype=torch.bfloat16, device=dev)
     ro_td, ids_td = u32(ro_t), torch.from_numpy(ids_t).to(dev)
-    ms = time_kernel(lambda: moeq.grouped_matmul_rowwise_fp8(c_t, a_t, b_t, sa_t, sb_t, ro_td,
-                                                             ids_td, 16), 20, batch=8)
-    out["fp8_rowwise_tiny_32x64x128"] = {"us": round(ms * 1e3, 2),
-                                         "timing": "median over 20 batches of 8 back-to-back calls"}
+    tiny = lambda: moeq.grouped_matmul_rowwise_fp8(c_t, a_t, b_t, sa_t, sb_t, ro_td, ids_td, 16)
+    ms = time_kernel(tiny, 20, batch=8)
+    # device-only: 64 launches captured in one CUDA graph, replayed; the
+    # per-launch time excludes the host's issue cost (ctypes marshalling,
+    # argument checks, cudaLaunchKernelEx)
+    n_graph = 64
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        tiny()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(n_graph):
+                tiny()
+    torch.cuda.current_stream().wait_stream(side)
+    ms_graph = time_kernel(g.replay, 20) / n_graph
+    out["fp8_rowwise_tiny_32x64x128"] = {
+        "us_per_call_binding": round(ms * 1e3, 2),
+        "us_device_per_launch": round(ms_graph * 1e3, 2),
+        "timing": "binding: median over 20 batches of 8 back-to-back calls through the Python "
+                  "binding; device: 64 launches in one CUDA graph, replay time / 64 "
+                  "(mean of 20 replays)"}
 
     # FP8 rowwise at MoE scale: 64 experts, 8192 tokens top-8 Zipf(1.1), K 7168, N 4096
     counts = synth.routing_counts(8192, 8, 64, seed=0, zipf_s=1.1)
@@ -319,7 +428,8 @@ def parts(pk, flush):
     fl = 2.0 * T * N * K
     out["fp8_rowwise_65536x4096x7168"] = {
         "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 1),
-        "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4)}
+        "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4),
+        "frac_fp8_nominal": round(fl / ms / 1e9 / NOMINAL["fp8_tflops"], 4)}
     del a, b, c
 
     # decode-shaped: 256 experts, 64 tokens top-8 -> 512 rows, K 7168, N 4096
@@ -335,7 +445,9 @@ def parts(pk, flush):
         c, a, b, sa, sb.reshape(256, N), ro_d, ids_d, int(counts.max())), 10)
     out["decode_fp8_rowwise_512rows_224experts"] = {
         "ms": round(ms, 4), "GB/s_active_weights": round(active_bytes / ms / 1e6, 1),
-        "frac_hbm": round(active_bytes / ms / 1e6 / hbm, 4), "active_experts": len(ids)}
+        "frac_hbm": round(active_bytes / ms / 1e6 / hbm, 4),
+        "frac_hbm_nominal": round(active_bytes / ms / 1e6 / NOMINAL["hbm_gbs"], 4),
+        "active_experts": len(ids)}
     del b
     rows = int(sum((int(cc) + 127) // 128 * 128 for cc in counts if cc))
     so_d = torch.empty(len(ids) + 1, dtype=torch.int32, device=dev)
@@ -349,7 +461,8 @@ def parts(pk, flush):
     wbytes = active_bytes + len(ids) * moeq.sf_bytes(N, K // 32)
     out["decode_mxfp8_512rows_224experts"] = {
         "ms": round(ms, 4), "GB/s_active_weights": round(wbytes / ms / 1e6, 1),
-        "frac_hbm": round(wbytes / ms / 1e6 / hbm, 4)}
+        "frac_hbm": round(wbytes / ms / 1e6 / hbm, 4),
+        "frac_hbm_nominal": round(wbytes / ms / 1e6 / NOMINAL["hbm_gbs"], 4)}
     del a, b8, c
     # single-rank expert dispatch: 16384 tokens routed top-8 over 128
     # experts, hidden 4096 -> 131072 MXFP4 rows (routing + gather-quantize)
@@ -387,8 +500,15 @@ def mx_part(d, pk):
     T, N, rows = d["T"], d["N"], d["rows"]
     a = torch.empty_like(d["a"])
     asf = torch.empty(moeq.sf_bytes(rows, K4 // 32), dtype=torch.uint8, device="cuda")
-    b = synth.random_fp4_packed((E4, N, K4 // 2), seed=501, device="cuda")
-    bsf = synth.random_bytes(E4 * moeq.sf_bytes(N, K4 // 32), 116, 126, seed=502, device="cuda")
+    # weights: bf16 N(0, 0.02) quantized to MXFP4 by the library, one group per expert
+    w = synth.bf16_normal((E4 * N, K4), 0.02, seed=501, device="cuda")
+    offs = torch.arange(E4 + 1, dtype=torch.int32, device="cuda") * N
+    eids = torch.arange(E4, dtype=torch.int32, device="cuda")
+    b = torch.empty((E4 * N, K4 // 2), dtype=torch.uint8, device="cuda")
+    bsf = torch.empty(moeq.sf_bytes(E4 * N, K4 // 32), dtype=torch.uint8, device="cuda")
+    moeq.grouped_quantize("mxfp4", w, b, bsf, offs, offs, eids, None, E4, E4 * N, N)
+    del w
+    b = b.view(E4, N, K4 // 2)
     c = torch.empty((T, I4 // 2), dtype=torch.uint8, device="cuda")
     csf = torch.empty(moeq.sf_bytes(rows, I4 // 32), dtype=torch.uint8, device="cuda")
 
@@ -404,7 +524,8 @@ def mx_part(d, pk):
     fl = flops_up(d)
     return {"quantize_mxfp4_ms": round(t_q, 4), "fused_gemm_swiglu_mxfp4_ms": round(t_f, 4),
             "fused_TFLOP/s": round(fl / t_f / 1e9, 1),
-            "fused_frac_fp4_peak": round(fl / t_f / 1e9 / (pk["bf16"] * FP4_OVER_BF16), 4)}
+            "fused_frac_fp4_peak": round(fl / t_f / 1e9 / (pk["bf16"] * FP4_OVER_BF16), 4),
+            "weights": "bf16 N(0, 0.02) quantized to MXFP4 by the library's grouped quantizer"}
 
 
 def chained_part(d, pk):
@@ -437,8 +558,7 @@ def layer_part(d):
     fused kernel's packed output and its padded scales."""
     from fp4_fp8_quantization_gb300 import moeq, synth
     H = K4
-    bd = synth.random_fp4_packed((E4, H, I4 // 2), seed=90, device="cuda")
-    bdsf = synth.random_bytes(E4 * moeq.sf_bytes(H, I4 // 16), 0x18, 0x28, seed=91, device="cuda")
+    bd, bdsf, _ = nvfp4_expert_weights(E4, H, I4, 0.02, 90)
     esd = synth.uniform((E4,), 0.5, 2.0, seed=92, device="cuda")
     out = torch.empty((d["T"], H), dtype=torch.bfloat16, device="cuda")
 
@@ -718,12 +838,21 @@ def run_moeq(args, rank, world):
     t_f = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     fp4_peak = pk["bf16"] * FP4_OVER_BF16
     achieved = fl / (t_f * 1e-3) / 1e12
+    traffic, traffic_note = fused_traffic_bytes()
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    mma_ceiling = FP4_FLOP_PER_SM_CYCLE * torch.cuda.get_device_properties(0).multi_processor_count \
+        * sm_mhz * 1e6 / 1e12
     roof = {"kernel": "grouped_gemm_kernel<NVFP4, fused SwiGLU>", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-            "frac": round(achieved / fp4_peak, 4), "traffic": FUSED_TRAFFIC_BYTES,
-            "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch "
-                            "of the current kernel (one ncu pass); null when not yet captured",
+            "frac": round(achieved / fp4_peak, 4), "traffic": traffic,
+            "traffic_note": traffic_note,
             "peak_note": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio",
+            "frac_nominal": round(achieved / NOMINAL["fp4_tflops"], 4),
+            "mma_ceiling": round(mma_ceiling, 1),
+            "frac_mma_ceiling": round(achieved / mma_ceiling, 4),
+            "mma_ceiling_note": "measured tcgen05 FP4 rate of this part (32768 flop per SM cycle: "
+                                "one M128xN256xK64 MMA per 128 cycles, 2x FP8, 4x bf16) x SMs x the "
+                                "run's median SM clock",
             "algorithmic_flops_per_launch": fl}
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
                  "fused_gemm_swiglu_ms": round(t_f, 4)}

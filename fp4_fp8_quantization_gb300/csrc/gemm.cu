@@ -259,6 +259,16 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
     }
 }
 
+// Bytes one CTA's loading warp l issues per stage in pair tiles (warp 0:
+// the A and B tiles, and the scale atoms too without a scale loader; the
+// scale loader: the A and all B scale atoms).
+template <class C>
+__device__ __forceinline__ uint32_t loader_bytes(int l) {
+    const uint32_t ab = C::A_BYTES + C::B_BYTES;
+    const uint32_t sf = C::SCALED ? C::SFA_BYTES + C::RB * C::SF_ATOMS * C::SF_ATOM_BYTES : 0u;
+    return C::SF_LOADER ? (l == 0 ? ab : sf) : ab + sf;
+}
+
 // Stores the NVFP4 scale bytes of `nblk` consecutive blocks (nblk = 1, 2 or
 // 4 chunks of 32 accumulator columns) starting at accumulator column nc0.
 __device__ __forceinline__ void store_sf_bytes(const Params &p, int64_t prow, int nc0,
@@ -398,6 +408,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ uint32_t prefix[kMaxGroups + 1];
+    // stages each loading warp of this CTA went through (announced on the
+    // barrier, copies issued), stored once when it stops; read by the even
+    // CTA at teardown
+    constexpr int LOADERS = 1 + C::SF_LOADER;
+    __shared__ uint32_t stages_done[LOADERS];
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -410,9 +425,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full_bar[s], 1 + C::SF_LOADER);  // one arrival per loading warp
+            // one arrival per loading warp (in a pair, the even CTA's
+            // loaders announce the bytes of both CTAs)
+            mbar_init(&full_bar[s], LOADERS);
             mbar_init(&empty_bar[s], 1);
         }
+#pragma unroll
+        for (int l = 0; l < LOADERS; ++l) stages_done[l] = 0;
 #pragma unroll
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             mbar_init(&tfull_bar[b], 1);
@@ -474,13 +493,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0 || (C::SF_LOADER && warp == 2)) {
         // ------------------------------------------------ TMA producers
         // Warp 0 loads the A and B tiles, warp 2 (or warp 0 as well, without
-        // a scale loader) the scale atoms; both arrive on the stage's full
-        // barrier with their byte counts.  Both CTAs of a pair load their own
-        // A rows, their half of the B rows and all of the tile's scales; the
-        // copies complete on the even CTA's full barrier, which expects the
-        // bytes of both.
+        // a scale loader) the scale atoms; each arrives on the stage's full
+        // barrier with its byte count and counts the stages it went through.
+        // Both CTAs of a pair load their own A rows, their half of the B
+        // rows and all of the tile's scales; the copies of both complete on
+        // the even CTA's full barrier, whose loaders expect the bytes of
+        // both CTAs (the odd CTA's loaders only issue).
         const bool do_ab = warp == 0;
         const bool do_sf = C::SCALED && (warp == 2 || !C::SF_LOADER);
+        const int loader = warp == 0 ? 0 : 1;
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b = policy_evict_last();
@@ -488,8 +509,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int nrb = (p.N + 127) / 128;
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued = 0;       // stages with a load issued
-            uint32_t issued_par = 0;   // phase parity of that load
+            uint32_t visits = 0;
             bool ok = true;
             for (uint32_t t = cid; ok && t < total; t += ncl) {
                 const Tile tl = decode_tile(prefix, G, t, NB);
@@ -528,8 +548,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // failure-detection test build: the first stage of the
                     // CTA's first tile is announced but never loaded, so every
                     // wait on it runs into its time limit
-                    stuck = !PAIRED && t == cid && kt == 0;
+                    stuck = t == cid && kt == 0;
 #endif
+                    ++visits;
                     if (!PAIRED) {
                         mbar_arrive_expect_tx(&full_bar[stage], tx);
                         if (do_ab && !stuck) {
@@ -547,12 +568,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     } else {
                         const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
                         if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2u * tx);
-                        if (do_ab) {
+                        if (do_ab && !stuck) {
                             tma_load_2d_pair(sa, &tmA, fb, kt * C::BK_BYTES, row0, pol_a);
                             tma_load_3d_pair(sb, &tmB, fb, kt * C::BK_BYTES,
                                              n0 + (int)rank * C::B_ROWS_CTA, e, pol_b);
                         }
-                        if (do_sf) {
+                        if (do_sf && !stuck) {
                             // scale buffers viewed as rows of 256 bytes: an
                             // atom is two rows
                             tma_load_2d_pair(ssfa, &tmSFA, fb, 0,
@@ -564,23 +585,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                              e * nrb + n0 / 128, pol_b);
                         }
                     }
-                    if (!stuck) {
-                        issued |= 1u << stage;
-                        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            // let every copy this CTA's barrier counts land before the CTA
-            // can exit (the odd CTA of a pair has none: its copies complete
-            // on the even CTA's barrier, which that CTA drains)
-            if (!ok && rank == 0) {
-                for (int s = 0; s < C::STAGES; ++s)
-                    if (issued & (1u << s)) mbar_drain(&full_bar[s], (issued_par >> s) & 1u);
-            }
+            stages_done[loader] = visits;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -788,6 +799,55 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // memory)
     pdl_trigger();
     tc_fence_before();
+    __syncthreads();
+    // every loader of both CTAs has stopped issuing
+    if (PAIRED) cluster_sync();
+    if (threadIdx.x == 0 && rank == 0) {
+        // Every issued copy lands before either CTA may leave, after an
+        // abort too.  No loader of either CTA reaches phase p + 1 of a stage
+        // before every loader reached phase p (it first waits for the MMAs
+        // that consumed phase p), so the counts differ by at most one and
+        // only the current phase n - 1 of a stage can be incomplete.  For it,
+        // each loader l of the even CTA that did not arrive arrives now,
+        // expecting the bytes of its odd-CTA counterpart if that one issued
+        // them; if the even loader arrived (expecting both CTAs' bytes) but
+        // its odd counterpart issued nothing, those bytes are completed
+        // here; then the phase is waited for with a bound.
+        uint32_t v0[LOADERS], v1[LOADERS];
+#pragma unroll
+        for (int l = 0; l < LOADERS; ++l) {
+            v0[l] = stages_done[l];
+            v1[l] = PAIRED ? ld_cluster_u32(mapa_shared(smem_u32(&stages_done[l]), 1)) : v0[l];
+        }
+        // phases of stage s a loader went through after v stages in all
+        auto phases = [](uint32_t v, int s) {
+            return v / C::STAGES + ((uint32_t)s < v % C::STAGES ? 1u : 0u);
+        };
+        for (int s = 0; s < C::STAGES; ++s) {
+            uint32_t c0[LOADERS], c1[LOADERS];
+            uint32_t n = 0;
+#pragma unroll
+            for (int l = 0; l < LOADERS; ++l) {
+                c0[l] = phases(v0[l], s);
+                c1[l] = phases(v1[l], s);
+                n = max(n, max(c0[l], c1[l]));
+            }
+            if (n == 0) continue;
+#pragma unroll
+            for (int l = 0; l < LOADERS; ++l) {
+                const uint32_t txl = loader_bytes<C>(l);
+                if (c0[l] < n) {
+                    if (PAIRED && c1[l] == n)
+                        mbar_arrive_expect_tx(&full_bar[s], txl);
+                    else
+                        mbar_arrive(&full_bar[s]);
+                } else if (PAIRED && c1[l] < n) {
+                    mbar_complete_tx(&full_bar[s], txl);
+                }
+            }
+            mbar_drain(&full_bar[s], (n - 1) & 1u);
+        }
+    }
     __syncthreads();
     // neither CTA of a pair leaves while the other may still target it
     if (PAIRED) cluster_sync();

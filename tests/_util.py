@@ -95,4 +95,29 @@ def sample_rows(a_offsets, n, seed=0):
     return np.array(sorted(rows), np.int64)
 
 
+def group_sample_rows(a_offsets, block=128):
+    """Per group (empty groups give an empty array): a row of its first
+    `block`-row m-block, one of its middle m-block and its last row -- all
+    rows of groups with at most 3."""
+    out = []
+    for g in range(len(a_offsets) - 1):
+        r0, r1 = int(a_offsets[g]), int(a_offsets[g + 1])
+        n = r1 - r0
+        if n <= 3:
+            out.append(np.arange(r0, r1, dtype=np.int64))
+            continue
+        nb = (n + block - 1) // block
+        mb = nb // 2
+        mid = r0 + mb * block + min(block // 2 + 5, n - 1 - mb * block)
+        out.append(np.array(sorted({r0 + min(5, n - 1), mid, r1 - 1}), np.int64))
+    return out
+
+
+def tile_sample_cols(N, tile=256, offsets=(0, 1, 31, 32, 63, 64, 127, 128, 159, 200, 254, 255)):
+    """Columns spread over every `tile`-wide n-tile of an N-column output
+    (first and last columns of the tile and of its 32-column chunks)."""
+    cols = {n0 + o for n0 in range(0, N, tile) for o in offsets if n0 + o < N}
+    return np.array(sorted(cols), np.int64)
+
+
 __all__ = ["synth"]

@@ -10,8 +10,10 @@ import torch
 
 from fp4_fp8_quantization_gb300 import moeq, synth
 from oracle import gemm as OG
-from tests._util import (DEV, assert_gemm_close, bf16_bits, groups_from_counts, need_gpu,
-                         sample_rows, to_dev_i32, to_dev_u32, u8)
+from oracle import layout as L
+from tests._util import (DEV, assert_gemm_close, bf16_bits, group_sample_rows,
+                         groups_from_counts, need_gpu, sample_rows, tile_sample_cols, to_dev_i32,
+                         to_dev_u32, u8)
 
 pytestmark = pytest.mark.gpu
 CANARY = -12288.0   # exactly representable in bf16
@@ -93,9 +95,58 @@ def test_rowwise_fp8_exact_invariants():
     assert np.array_equal(cp, c1[idx])
 
 
+def _full_width_groups(ro):
+    """Groups checked over every output column: the first, the largest, the
+    smallest non-empty and the last."""
+    n = np.diff(ro.astype(np.int64))
+    nz = np.nonzero(n)[0]
+    return sorted({int(nz[0]), int(np.argmax(n)), int(nz[np.argmin(n[nz])]), int(nz[-1])})
+
+
+def _all_rows(ro):
+    return [np.arange(int(ro[g]), int(ro[g + 1]), dtype=np.int64) for g in range(len(ro) - 1)]
+
+
+def _rows_cols(t, rows, cols=None):
+    """uint8 numpy copy of t[rows] (and [:, cols]), gathered on the device."""
+    if t.dtype != torch.uint8:
+        t = t.view(torch.uint8)
+    idx = torch.from_numpy(np.asarray(rows, np.int64)).to(t.device)
+    sub = t.index_select(0, idx)
+    if cols is not None:
+        sub = sub.index_select(1, torch.from_numpy(np.asarray(cols, np.int64)).to(t.device))
+    return u8(sub)
+
+
+def _check_rowwise_sampled(c, a, sa, b, sb, ro, ids, N, tile, all_rows=False):
+    """Every non-empty group: rows of its first, middle and last m-block (or
+    all its rows) against the oracle, on columns spread over every n-tile
+    (all columns for a few groups).  Tensors on the device: c [T, N] bf16,
+    a [T, K] e4m3, sa [T], b [E, N, K] e4m3, sb [E, N]."""
+    cols = tile_sample_cols(N, tile)
+    full = _full_width_groups(ro)
+    checked = 0
+    sa_np = sa.cpu().numpy()
+    for g, rows in enumerate(_all_rows(ro) if all_rows else group_sample_rows(ro)):
+        if rows.size == 0:
+            continue
+        e = int(ids[g])
+        cc = np.arange(N) if g in full else cols
+        _, f64 = OG.grouped_matmul_rowwise_fp8(_rows_cols(a, rows), _rows_cols(b[e], cc)[None],
+                                               sa_np[rows], sb[e:e + 1, torch.from_numpy(cc).to(
+                                                   sb.device)].cpu().numpy(),
+                                               np.array([0, len(rows)], np.uint32), [0],
+                                               return_f64=True)
+        got = bf16_bits(c.index_select(0, torch.from_numpy(rows).to(c.device)))[:, cc]
+        assert_gemm_close(got, f64)
+        checked += 1
+    assert checked == int((np.diff(ro.astype(np.int64)) > 0).sum())
+
+
 def test_rowwise_fp8_moe_scale_sampled():
     """64 experts, 8192 tokens top-8 with Zipf(1.1) popularity -> 65536 rows,
-    K = 7168, N = 4096; sampled rows of every group."""
+    K = 7168, N = 4096: every group on rows of its first, middle and last
+    m-block."""
     need_gpu()
     counts = synth.routing_counts(8192, 8, 64, seed=0, zipf_s=1.1)
     ro, ids = synth.ragged_groups(counts)
@@ -106,21 +157,12 @@ def test_rowwise_fp8_moe_scale_sampled():
     moeq.grouped_matmul_rowwise_fp8(c, a, b, sa, sb.reshape(E, N), to_dev_u32(ro),
                                     to_dev_i32(ids), max_tokens_per_expert=int(counts.max()))
     torch.cuda.synchronize()
-    rows = sample_rows(ro, 96, seed=3)
-    grp = np.searchsorted(ro, rows, side="right") - 1
-    a_s, sa_s, c_s = u8(a)[rows], sa.cpu().numpy()[rows], bf16_bits(c)[rows]
-    b_np, sb_np = u8(b), sb.reshape(E, N).cpu().numpy()
-    for g in np.unique(grp)[::2]:
-        m = grp == g
-        sub_ro = np.array([0, m.sum()], np.uint32)
-        e = int(ids[g])
-        _, f64 = OG.grouped_matmul_rowwise_fp8(a_s[m], b_np[e:e + 1], sa_s[m], sb_np[e:e + 1],
-                                               sub_ro, [0], return_f64=True)
-        assert_gemm_close(c_s[m], f64)
+    _check_rowwise_sampled(c, a, sa, b, sb.reshape(E, N), ro, ids, N, 256)
 
 
 def test_rowwise_fp8_decode_shape_sampled():
-    """256 experts, 64 tokens top-8 -> 512 rows over ~224 experts of 1-7 rows."""
+    """256 experts, 64 tokens top-8 -> 512 rows over ~224 experts of 1-7 rows:
+    every group, all its rows."""
     need_gpu()
     counts = synth.routing_counts(64, 8, 256, seed=0)
     ro, ids = synth.ragged_groups(counts)
@@ -131,14 +173,7 @@ def test_rowwise_fp8_decode_shape_sampled():
     moeq.grouped_matmul_rowwise_fp8(c, a, b, sa, sb.reshape(E, N), to_dev_u32(ro),
                                     to_dev_i32(ids), max_tokens_per_expert=int(counts.max()))
     torch.cuda.synchronize()
-    gsel = np.linspace(0, len(ids) - 1, 24).astype(int)
-    a_np, sa_np, c_np = u8(a), sa.cpu().numpy(), bf16_bits(c)
-    for g in gsel:
-        e, r0, r1 = int(ids[g]), int(ro[g]), int(ro[g + 1])
-        _, f64 = OG.grouped_matmul_rowwise_fp8(
-            a_np[r0:r1], u8(b[e:e + 1]), sa_np[r0:r1], sb.reshape(E, N)[e:e + 1].cpu().numpy(),
-            np.array([0, r1 - r0], np.uint32), [0], return_f64=True)
-        assert_gemm_close(c_np[r0:r1], f64)
+    _check_rowwise_sampled(c, a, sa, b, sb.reshape(E, N), ro, ids, N, 256, all_rows=True)
 
 
 def test_rowwise_fp8_bad_expert_skips_group():
@@ -230,38 +265,56 @@ def _cfg4_groups(seed=0):
     return counts, ro, ids, so
 
 
+def _check_blockscaled_sampled(fmt, c, a, asf_np, b, bsf_np, es_np, ro, so, ids, N, K,
+                               tile, all_rows=False):
+    """Every non-empty group: rows of its first, middle and last m-block (or
+    all its rows) against the oracle, each as a one-group problem over its
+    own scale rows and the sampled weight rows (columns) with theirs.  c, a,
+    b on the device; the scale buffers as numpy bytes."""
+    v = 16 if fmt == "nvfp4" else 32
+    kv = K // v
+    per = moeq.sf_bytes(N, kv)
+    cols = tile_sample_cols(N, tile)
+    full = _full_width_groups(ro)
+    kcols = np.arange(kv)[None, :]
+    checked = 0
+    for g, rows in enumerate(_all_rows(ro) if all_rows else group_sample_rows(ro)):
+        if rows.size == 0:
+            continue
+        e = int(ids[g])
+        cc = np.arange(N) if g in full else cols
+        prow = int(so[g]) + rows - int(ro[g])
+        pad = np.zeros((128, kv), np.uint8)
+        pad[:len(rows)] = asf_np[L.sf_offset(prow[:, None], kcols, kv)]
+        bsf_e = bsf_np[e * per:(e + 1) * per]
+        sub_bsf = L.swizzle(bsf_e[L.sf_offset(cc[:, None], kcols, kv)])
+        _, f64 = OG.grouped_matmul_blockscaled(
+            fmt, _rows_cols(a, rows), L.swizzle(pad), _rows_cols(b[e], cc)[None], sub_bsf,
+            None if es_np is None else es_np[e:e + 1], np.array([0, len(rows)], np.uint32),
+            np.array([0, 128], np.uint32), [0], N=len(cc), K=K, scale_rows_total=128,
+            return_f64=True)
+        got = bf16_bits(c.index_select(0, torch.from_numpy(rows).to(c.device)))[:, cc]
+        assert_gemm_close(got, f64)
+        checked += 1
+    assert checked == int((np.diff(ro.astype(np.int64)) > 0).sum())
+
+
 def test_nvfp4_blockscaled_moe_scale_sampled():
-    """128 experts, 16384 tokens top-8 -> 131072 rows, K = 4096, N = 3072."""
+    """128 experts, 16384 tokens top-8 -> 131072 rows, K = 4096, N = 3072:
+    every group on rows of its first, middle and last m-block."""
     need_gpu()
     counts, ro, ids, so = _cfg4_groups()
     T, E, N, K = int(ro[-1]), 128, 3072, 4096
     rows = int(so[-1])
     a, asf, b, bsf, es = blockscaled_inputs("nvfp4", T, E, N, K, rows, seed=40, device=DEV)
-    c = bf16_bits(run_blockscaled("nvfp4", a, asf, b, bsf, es, ro, so, ids, N, K, rows))
-    sel = sample_rows(ro, 64, seed=5)
-    grp = np.searchsorted(ro, sel, side="right") - 1
-    a_np, asf_np, bsf_np, es_np = u8(a), u8(asf), u8(bsf), es.cpu().numpy()
-    per = moeq.sf_bytes(N, K // 16)
-    for g in np.unique(grp)[:24]:
-        e = int(ids[g])
-        rr = sel[grp == g]
-        # the oracle on just these rows: a one-group problem with the group's scale rows
-        sub_ro = np.array([0, len(rr)], np.uint32)
-        a_sub = a_np[rr]
-        from oracle import layout as L
-        kv = K // 16
-        sa_log = L.unswizzle(asf_np, rows, kv)[int(so[g]) + rr - int(ro[g])]
-        pad = np.zeros((128, kv), np.uint8)
-        pad[:len(rr)] = sa_log
-        _, f64 = OG.grouped_matmul_blockscaled(
-            "nvfp4", a_sub, L.swizzle(pad), u8(b[e:e + 1]), bsf_np[e * per:(e + 1) * per],
-            es_np[e:e + 1], sub_ro, np.array([0, 128], np.uint32), [0], N=N, K=K,
-            scale_rows_total=128, return_f64=True)
-        assert_gemm_close(c[rr], f64)
+    c = run_blockscaled("nvfp4", a, asf, b, bsf, es, ro, so, ids, N, K, rows)
+    _check_blockscaled_sampled("nvfp4", c, a, u8(asf), b, u8(bsf), es.cpu().numpy(),
+                               ro, so, ids, N, K, 256)
 
 
 def test_mxfp8_decode_shape_sampled():
-    """256 experts, 64 tokens top-8 -> 512 rows, K = 7168, N = 4096, MXFP8."""
+    """256 experts, 64 tokens top-8 -> 512 rows, K = 7168, N = 4096, MXFP8:
+    every group, all its rows."""
     need_gpu()
     from oracle import quantize as Q
     counts = synth.routing_counts(64, 8, 256, seed=0)
@@ -270,42 +323,21 @@ def test_mxfp8_decode_shape_sampled():
     T, E, N, K = int(ro[-1]), 256, 4096, 7168
     rows = int(so[-1])
     a, asf, b, bsf, _ = blockscaled_inputs("mxfp8", T, E, N, K, rows, seed=50, device=DEV)
-    c = bf16_bits(run_blockscaled("mxfp8", a, asf, b, bsf, None, ro, so, ids, N, K, rows))
-    per = moeq.sf_bytes(N, K // 32)
-    a_np, asf_np, bsf_np = u8(a), u8(asf), u8(bsf)
-    from oracle import layout as L
-    lg = L.unswizzle(asf_np, rows, K // 32)
-    for g in np.linspace(0, len(ids) - 1, 16).astype(int):
-        e, r0, r1 = int(ids[g]), int(ro[g]), int(ro[g + 1])
-        pad = np.zeros((128, K // 32), np.uint8)
-        pad[:r1 - r0] = lg[int(so[g]):int(so[g]) + r1 - r0]
-        _, f64 = OG.grouped_matmul_blockscaled(
-            "mxfp8", a_np[r0:r1], L.swizzle(pad), u8(b[e:e + 1]), bsf_np[e * per:(e + 1) * per],
-            None, np.array([0, r1 - r0], np.uint32), np.array([0, 128], np.uint32), [0],
-            N=N, K=K, scale_rows_total=128, return_f64=True)
-        assert_gemm_close(c[r0:r1], f64)
+    c = run_blockscaled("mxfp8", a, asf, b, bsf, None, ro, so, ids, N, K, rows)
+    _check_blockscaled_sampled("mxfp8", c, a, u8(asf), b, u8(bsf), None, ro, so, ids,
+                               N, K, 128, all_rows=True)
 
 
 def test_mxfp4_blockscaled_moe_scale_sampled():
-    """MXFP4 at the 128-expert shape (K = 4096, N = 3072), sampled rows."""
+    """MXFP4 at the 128-expert shape (K = 4096, N = 3072): every group on rows
+    of its first, middle and last m-block."""
     need_gpu()
-    from oracle import layout as L
     counts, ro, ids, so = _cfg4_groups(seed=1)
     T, E, N, K = int(ro[-1]), 128, 3072, 4096
     rows = int(so[-1])
     a, asf, b, bsf, _ = blockscaled_inputs("mxfp4", T, E, N, K, rows, seed=45, device=DEV)
-    c = bf16_bits(run_blockscaled("mxfp4", a, asf, b, bsf, None, ro, so, ids, N, K, rows))
-    kv = K // 32
-    per = moeq.sf_bytes(N, kv)
-    a_np, bsf_np = u8(a), u8(bsf)
-    lg = L.unswizzle(u8(asf), rows, kv)
-    for g in np.linspace(0, len(ids) - 1, 12).astype(int):
-        e, r0 = int(ids[g]), int(ro[g])
-        rr = np.arange(r0, min(r0 + 3, int(ro[g + 1])))
-        pad = np.zeros((128, kv), np.uint8)
-        pad[:len(rr)] = lg[int(so[g]) + rr - r0]
-        _, f64 = OG.grouped_matmul_blockscaled(
-            "mxfp4", a_np[rr], L.swizzle(pad), u8(b[e:e + 1]), bsf_np[e * per:(e + 1) * per], None,
-            np.array([0, len(rr)], np.uint32), np.array([0, 128], np.uint32), [0], N=N, K=K,
-            scale_rows_total=128, return_f64=True)
-        assert_gemm_close(c[rr], f64)
+    c = run_blockscaled("mxfp4", a, asf, b, bsf, None, ro, so, ids, N, K, rows)
+    _check_blockscaled_sampled("mxfp4", c, a, u8(asf), b, u8(bsf), None, ro, so, ids,
+                               N, K, 256)
+
+
