@@ -29,6 +29,12 @@ namespace {
 #ifndef MOEQ_QUANT_U
 #define MOEQ_QUANT_U 4
 #endif
+// NVFP4 rows: a rolling window of 32-byte loads per lane (the load of step
+// s + W is issued as soon as step s is consumed).  3 in flight: 17.8 us on
+// 8192 x 4096 rows against 18.4 us with 4 (same box, back-to-back calls).
+#ifndef MOEQ_QUANT_W_NVFP4
+#define MOEQ_QUANT_W_NVFP4 3
+#endif
 #ifndef MOEQ_Q_MINB
 #define MOEQ_Q_MINB 8
 #endif
@@ -390,28 +396,43 @@ __device__ __forceinline__ void load_step(const uint8_t *a, uint32_t (&w)[8]) {
     }
 }
 
+// Entry c of the NVFP4 multiplier table: inv / value(c) for the E4M3 scale
+// code c, 0 for the zero code (and the NaN code, never produced).
+__device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
+    return (c == 0 || c >= 0x7F) ? 0.0f : __fdiv_rn(inv, e4m3_pos_value(c));
+}
+
 // NVFP4 quantization of one row of K bf16 (one warp): lane i takes elements
 // [16 i, 16 i + 16) of each 512-element step, a whole block.  Codes go to
-// out_row, the E4M3 block scales to logical scale row prow.  r_tab[c] =
-// inv / value(c) for every E4M3 code c (0 where the block scale is 0).
+// out_row, the E4M3 block scales to logical scale row prow.  The row's
+// multiplier table r_tab[c] = inv / value(c) for every E4M3 code c (0 where
+// the block scale is 0; the same IEEE division per entry as the block rule)
+// is built while the row's first loads are in flight.
 template <bool A32>
 __device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *out_row,
                                                    uint8_t *scales, int64_t prow, int64_t K,
-                                                   float inv, const float *r_tab, int lane) {
+                                                   float tscale, float *r_tab, int lane) {
     const int64_t kv_atoms = K / 64;
     const int nsteps = (int)((K + 511) / 512);
     const int lanes_last = (int)(K / 16 - (int64_t)(nsteps - 1) * 32);
-    constexpr int U = MOEQ_QUANT_U;  // 32-byte loads in flight per lane
+    constexpr int U = MOEQ_QUANT_W_NVFP4;  // 32-byte loads in flight per lane
+    // rolling window: step s is loaded into w[s % U]; once it is consumed,
+    // the load of step s + U goes into the same registers
+    uint32_t w[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+        if (u < nsteps && (u < nsteps - 1 || lane < lanes_last))
+            load_step<A32>(src + (int64_t)u * 1024 + lane * 32, w[u]);
+    }
+    // the row's inverse tensor scale and multiplier table, while the first
+    // loads are in flight
+    const float inv = __fdiv_rn(1.0f, tscale);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r_tab[lane * 4 + j] = nvfp4_r_entry(lane * 4 + j, inv);
+    __syncwarp();
     for (int s0 = 0; s0 < nsteps; s0 += U) {
-        uint32_t w[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
-            const int s = s0 + u;
-            if (s < nsteps && (s < nsteps - 1 || lane < lanes_last))
-                load_step<A32>(src + (int64_t)s * 1024 + lane * 32, w[u]);
-        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int s = s0 + u;
@@ -431,6 +452,11 @@ __device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *
                 }
                 codes[h] = nvfp4_codes8(x, r);
             }
+            const int sn = s + U;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+            if (sn < nsteps && (sn < nsteps - 1 || lane < lanes_last))
+                load_step<A32>(src + (int64_t)sn * 1024 + lane * 32, w[u]);
             const uint32_t word = gather4(sc0.code, lane, 1);
             if (!active) continue;
             reinterpret_cast<uint2 *>(out_row)[s * 32 + lane] = make_uint2(codes[0], codes[1]);
@@ -441,11 +467,6 @@ __device__ __forceinline__ void nvfp4_quantize_row(const uint8_t *src, uint8_t *
     }
 }
 
-// Entry c of the NVFP4 multiplier table: inv / value(c) for the E4M3 scale
-// code c, 0 for the zero code (and the NaN code, never produced).
-__device__ __forceinline__ float nvfp4_r_entry(uint32_t c, float inv) {
-    return (c == 0 || c >= 0x7F) ? 0.0f : __fdiv_rn(inv, e4m3_pos_value(c));
-}
 
 // fmt: 0 NVFP4, 1 MXFP4, 2 MXFP8.  One warp per logical scale row; in each
 // 512-element step lane i takes elements [16 i, 16 i + 16): a whole NVFP4
@@ -479,13 +500,8 @@ __global__ void __launch_bounds__(kQWarps * 32, MOEQ_Q_MINB) quantize_kernel(Qua
     if (srow < 0) return;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(p.in + srow * p.stride);
     if (FMT == 0) {
-        // r depends only on the block's E4M3 scale code: tabulate
-        // r[c] = inv / value(c) once per row (same IEEE division per entry).
-        const float inv = __fdiv_rn(1.0f, gv.scale(gi));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) r_table[wid][lane * 4 + j] = nvfp4_r_entry(lane * 4 + j, inv);
-        __syncwarp();
-        nvfp4_quantize_row<A32>(src, p.out + row * (p.K / 2), p.scales, prow, p.K, inv,
+        // r depends only on the block's E4M3 scale code: tabulated per row
+        nvfp4_quantize_row<A32>(src, p.out + row * (p.K / 2), p.scales, prow, p.K, gv.scale(gi),
                                 r_table[wid], lane);
         return;
     }
