@@ -228,17 +228,16 @@ def swiglu_output_scales(y, ro, ids, num_experts):
     / 2688 (1 for an empty or all-zero group).  PyTorch's fp32 SiLU stands in
     for the library's here: the result is an input scale, valid at any
     positive value."""
-    out = torch.ones(num_experts, dtype=torch.float32, device=y.device)
-    for g in range(len(ids)):
-        r0, r1 = int(ro[g]), int(ro[g + 1])
-        if r1 == r0:
-            continue
-        yy = y[r0:r1].float()
-        h = torch.nn.functional.silu(yy[:, 0::2]) * yy[:, 1::2]
-        amax = float(h.abs().max())
-        if amax > 0:
-            out[int(ids[g])] = float(np.float32(amax) / np.float32(2688.0))
-    return out
+    dev = y.device
+    h = torch.nn.functional.silu(y[:, 0::2].float()).mul_(y[:, 1::2].float()).abs_()
+    rowmax = h.amax(dim=1)
+    del h
+    counts = torch.from_numpy(np.diff(ro.astype(np.int64))).to(dev)
+    expert_of_row = torch.repeat_interleave(torch.from_numpy(ids.astype(np.int64)).to(dev), counts)
+    emax = torch.zeros(num_experts, dtype=torch.float32, device=dev)
+    emax.scatter_reduce_(0, expert_of_row, rowmax, reduce="amax")
+    scale = (emax / torch.tensor(2688.0, dtype=torch.float32, device=dev))
+    return torch.where(emax > 0, scale, torch.ones_like(scale))
 
 
 def up_projection_inputs(seed, device="cuda"):
