@@ -63,6 +63,16 @@ constexpr int kQWarps = MOEQ_Q_WARPS;
 #define MOEQ_S_MINB 10
 #endif
 constexpr int kSWarps = MOEQ_S_WARPS;
+// chained SwiGLU + NVFP4: scale rows per warp, min CTAs per SM (at most 64
+// registers).  On 131072 x 3072: 0.230 ms with 2 rows per warp, 0.233 ms
+// with 1, 0.234 / 0.238 ms with 4 / 8 (the 8-h-per-lane kernel above:
+// 0.291 ms on the same GPU).
+#ifndef MOEQ_SN_RPW
+#define MOEQ_SN_RPW 2
+#endif
+#ifndef MOEQ_SN_MINB
+#define MOEQ_SN_MINB 8
+#endif
 
 // The group description, read either from a per-CTA shared-memory copy
 // (up to kTableCap groups: one coalesced round trip per CTA instead of a
@@ -780,21 +790,155 @@ struct SwigluParams {
     uint32_t *err;
 };
 
-// One warp per logical scale row; a lane takes 8 (gate, up) pairs = 8 h
-// values per 256-h step.  OUT: 0 NVFP4 (a 16-h block is held by lanes 2i,
-// 2i+1), 1 MXFP4 / 2 MXFP8 (a 32-h block by lanes 4i .. 4i+3).
+// SwiGLU + NVFP4 requant of one row of y (one warp).  In each 512-h step
+// lane i takes the (gate, up) pairs of h [16 i, 16 i + 16), one whole NVFP4
+// block: 64 bytes of y, read as two 32-byte loads (four 16-byte loads when
+// y is not 32-byte aligned).  The loads of step s + 1 are issued as soon as
+// the pairs of step s are turned into h, so they are in flight while step s
+// is quantized.  r_tab is the row group's multiplier table (entry c = inv /
+// value(c), 0 where value(c) is 0: the division of the block rule, once per
+// code).  Codes go to out_row (8 bytes per lane and step), the E4M3 block
+// scales to logical scale row prow (one 4-byte word per 4 lanes).
+template <bool A32>
+__device__ __forceinline__ void swiglu_nvfp4_row(const uint8_t *src, uint8_t *out_row,
+                                                 uint8_t *scales, int64_t prow, int nh,
+                                                 int64_t kv_atoms, float inv,
+                                                 const float *r_tab, int lane) {
+    const int nsteps = (nh + 511) >> 9;
+    const int lanes_last = (nh - ((nsteps - 1) << 9)) >> 4;  // nh is a multiple of 64
+    auto load = [&](int s, uint32_t (&d)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) d[i] = 0u;
+        if (s >= nsteps || (s == nsteps - 1 && lane >= lanes_last)) return;
+        const uint8_t *a = src + ((int64_t)s << 11) + lane * 64;
+        if (A32) {
+            ld_stream32(a, *reinterpret_cast<uint32_t(*)[8]>(&d[0]));
+            ld_stream32(a + 32, *reinterpret_cast<uint32_t(*)[8]>(&d[8]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = ld_stream(a + 16 * k);
+                d[4 * k] = v.x;
+                d[4 * k + 1] = v.y;
+                d[4 * k + 2] = v.z;
+                d[4 * k + 3] = v.w;
+            }
+        }
+    };
+    uint32_t w[16];
+    load(0, w);
+    // the scale word of blocks [4 kb, 4 kb + 4) of this row is at sf0 + 512 kb
+    const int64_t sf0 = sf_word_offset(prow, 0, kv_atoms);
+    for (int s = 0; s < nsteps; ++s) {
+        const bool active = s < nsteps - 1 || lane < lanes_last;
+        float h[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {  // word i: gate_i in the low half, up_i in the high
+            const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
+                                  bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
+                                  __uint_as_float(w[i] & 0xFFFF0000u),
+                                  __uint_as_float(w[i + 1] & 0xFFFF0000u));
+            h[i] = f2_lo(hh);
+            h[i + 1] = f2_hi(hh);
+        }
+        load(s + 1, w);
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(h[i]));
+        const uint32_t code = nvfp4_block_scale_code(m, inv).code;
+        const float r = r_tab[code & 0x7Fu];
+        float lo8[8], hi8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo8[i] = h[i];
+            hi8[i] = h[8 + i];
+        }
+        const uint32_t c0 = nvfp4_codes8(lo8, r);
+        const uint32_t c1 = nvfp4_codes8(hi8, r);
+        // lanes 4j .. 4j+3 hold the scale bytes of one word
+        uint32_t word = code << (8 * (lane & 3));
+        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
+        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+        if (!active) continue;
+        reinterpret_cast<uint2 *>(out_row)[s * 32 + lane] = make_uint2(c0, c1);
+        if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t *>(scales + sf0 + (int64_t)(s * 8 + (lane >> 2)) * 512) =
+                word;
+    }
+}
+
+// Chained SwiGLU + NVFP4: each warp takes MOEQ_SN_RPW consecutive logical
+// scale rows, looking their group up (and building its multiplier table)
+// only when a row leaves the group of the previous one.
+__global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_nvfp4_kernel(SwigluParams p) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float r_tables[kSWarps][128];
+    __shared__ GroupTable table;
+    const GroupView gv = load_groups(p.g, p.out_tensor_scale, table);
+    const int lane = threadIdx.x & 31;
+    float *r_tab = r_tables[threadIdx.x >> 5];
+    const int64_t kv_atoms = p.I / 64;
+    const bool a32 = (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
+    const int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
+    int gi = -1;
+    uint32_t s0 = 0, s1 = 0, r0 = 0, rg = 0;
+    float inv = 0.0f;
+    for (int k = 0; k < MOEQ_SN_RPW; ++k) {
+        const int64_t prow = prow0 + k;  // warp-uniform
+        if (prow >= p.g.scale_rows_total) return;
+        if (gi < 0 || (uint32_t)prow < s0 || (uint32_t)prow >= s1) {
+            gi = scale_row_group(gv, (uint32_t)prow, p.err);
+            if (gi < 0) continue;
+            s0 = gv.so[gi];
+            s1 = gv.so[gi + 1];
+            r0 = gv.ro[gi];
+            rg = gv.ro[gi + 1] - r0;
+            inv = __fdiv_rn(1.0f, gv.scale(gi));
+            __syncwarp();  // every lane is done with the previous table
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t c = (uint32_t)(lane * 4 + j);
+                const float v = e4m3_pos_value(c);
+                r_tab[c] = v == 0.0f ? 0.0f : __fdiv_rn(inv, v);
+            }
+            __syncwarp();
+        }
+        const uint32_t local = (uint32_t)prow - s0;
+        if (local >= rg) {  // padding row of the group
+            if (local < ((rg + 127u) & ~127u) && store_ok(prow < p.g.scale_rows_total, p.err))
+                zero_scale_row(p.scales, prow, kv_atoms, lane);
+            continue;
+        }
+        const int64_t row = (int64_t)r0 + local;
+        if (!store_ok(row < p.g.total_rows, p.err)) continue;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.y + row * 2 * p.I);
+        uint8_t *out_row = p.out + row * (p.I / 2);
+        if (a32)
+            swiglu_nvfp4_row<true>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, inv, r_tab,
+                                   lane);
+        else
+            swiglu_nvfp4_row<false>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, inv, r_tab,
+                                    lane);
+    }
+}
+
+// Chained SwiGLU + MX requant: one warp per logical scale row; a lane takes
+// 8 (gate, up) pairs = 8 h values per 256-h step, a 32-h block is held by
+// lanes 4i .. 4i+3.  OUT: 1 MXFP4, 2 MXFP8.
 template <int OUT>
-__global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_kernel(SwigluParams p) {
+__global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_mx_kernel(SwigluParams p) {
+    static_assert(OUT == 1 || OUT == 2, "MX output formats");
     pdl_wait();
     pdl_trigger();
     __shared__ GroupTable table;
-    const GroupView gv = load_groups(p.g, OUT == 0 ? p.out_tensor_scale : nullptr, table);
+    const GroupView gv = load_groups(p.g, nullptr, table);
     const int lane = threadIdx.x & 31;
     const int64_t prow = (int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5);
     if (prow >= p.g.scale_rows_total) return;
     const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
     if (gi < 0) return;
-    const int64_t kv_atoms = OUT == 0 ? p.I / 64 : p.I / 128;
+    const int64_t kv_atoms = p.I / 128;
     const uint32_t r0 = gv.ro[gi];
     const uint32_t rg = gv.ro[gi + 1] - r0;
     const uint32_t local = (uint32_t)prow - gv.so[gi];
@@ -805,7 +949,6 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_ker
     }
     const int64_t row = (int64_t)r0 + local;
     if (!store_ok(row < p.g.total_rows && prow < p.g.scale_rows_total, p.err)) return;
-    const float inv = OUT == 0 ? __fdiv_rn(1.0f, gv.scale(gi)) : 0.0f;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
     const int64_t nh = p.I;
     constexpr int U = MOEQ_S_U;  // 256-h steps whose loads are issued together
@@ -846,47 +989,35 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_quantize_ker
 #pragma unroll
         for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(h[i]));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        if (OUT == 0) {
-            Nvfp4Scale s = nvfp4_block_scale(m, inv);
-            uint32_t codes = nvfp4_codes8(h, s.r);
-            uint32_t word = gather4(s.code, lane, 2);
-            if (active) {
-                reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = codes;
-                if ((lane & 7) == 0)
-                    *reinterpret_cast<uint32_t *>(
-                        p.scales + sf_word_offset(prow, hl / 64, kv_atoms)) = word;
-            }
-        } else {
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));  // the block's 4 lanes
-            uint32_t code = 0;
-            float f = 0.0f;
-            if (m != 0.0f) {
-                code = mx_scale_code_f32(m, OUT == 2 ? 8 : 2);
-                f = mx_multiplier(code);
-            }
-            float q[8];
-            const F2 f2v = f2(f, f);
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));  // the block's 4 lanes
+        uint32_t code = 0;
+        float f = 0.0f;
+        if (m != 0.0f) {
+            code = mx_scale_code_f32(m, OUT == 2 ? 8 : 2);
+            f = mx_multiplier(code);
+        }
+        float q[8];
+        const F2 f2v = f2(f, f);
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const F2 t = mul2(f2(h[i], h[i + 1]), f2v);
-                q[i] = f2_lo(t);
-                q[i + 1] = f2_hi(t);
+        for (int i = 0; i < 8; i += 2) {
+            const F2 t = mul2(f2(h[i], h[i + 1]), f2v);
+            q[i] = f2_lo(t);
+            q[i + 1] = f2_hi(t);
+        }
+        const uint32_t word = gather4(code, lane, 4);
+        if (active) {
+            if (OUT == 2) {
+                uint2 o = make_uint2(e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16),
+                                     e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16));
+                if (m == 0.0f) o = make_uint2(0u, 0u);  // all-zero block: +0 codes
+                *reinterpret_cast<uint2 *>(p.out + row * p.I + hl) = o;
+            } else {
+                const uint32_t o = m == 0.0f ? 0u : e2m1x8(q);
+                reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = o;
             }
-            const uint32_t word = gather4(code, lane, 4);
-            if (active) {
-                if (OUT == 2) {
-                    uint2 o = make_uint2(e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16),
-                                         e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16));
-                    if (m == 0.0f) o = make_uint2(0u, 0u);  // all-zero block: +0 codes
-                    *reinterpret_cast<uint2 *>(p.out + row * p.I + hl) = o;
-                } else {
-                    const uint32_t o = m == 0.0f ? 0u : e2m1x8(q);
-                    reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = o;
-                }
-                if ((lane & 15) == 0)
-                    *reinterpret_cast<uint32_t *>(
-                        p.scales + sf_word_offset(prow, hl / 128, kv_atoms)) = word;
-            }
+            if ((lane & 15) == 0)
+                *reinterpret_cast<uint32_t *>(
+                    p.scales + sf_word_offset(prow, hl / 128, kv_atoms)) = word;
         }
       }
     }
@@ -1009,12 +1140,16 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
                                    int64_t I, const float *out_tensor_scale, const GroupArgs &g,
                                    uint32_t *err, cudaStream_t s) {
     SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
-    int64_t blocks = (g.scale_rows_total + kSWarps - 1) / kSWarps;
-    if (blocks == 0) return cudaSuccess;
-    void (*kern)(SwigluParams) = out_fmt == 0   ? swiglu_quantize_kernel<0>
-                                 : out_fmt == 1 ? swiglu_quantize_kernel<1>
-                                                : swiglu_quantize_kernel<2>;
-    return launch_pdl(kern, (unsigned)blocks, kSWarps * 32, 0, s, p);
+    if (g.scale_rows_total == 0) return cudaSuccess;
+    if (out_fmt == 0) {
+        const int64_t per_cta = (int64_t)kSWarps * MOEQ_SN_RPW;
+        return launch_pdl(swiglu_nvfp4_kernel,
+                          (unsigned)((g.scale_rows_total + per_cta - 1) / per_cta), kSWarps * 32,
+                          0, s, p);
+    }
+    const int64_t blocks = (g.scale_rows_total + kSWarps - 1) / kSWarps;
+    return launch_pdl(out_fmt == 1 ? swiglu_mx_kernel<1> : swiglu_mx_kernel<2>, (unsigned)blocks,
+                      kSWarps * 32, 0, s, p);
 }
 
 }  // namespace moeq

@@ -13,7 +13,8 @@ from fp4_fp8_quantization_gb300 import moeq, synth
 from oracle import layout as L
 from oracle import quantize as Q
 from oracle import swiglu as S
-from tests._util import DEV, groups_from_counts, need_gpu, sample_rows, to_dev_i32, to_dev_u32, u8
+from tests._util import (DEV, group_sample_rows, groups_from_counts, need_gpu, to_dev_i32,
+                         to_dev_u32, u8)
 from tests.test_gpu_gemm import blockscaled_inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +31,7 @@ def _run_chained_swiglu(y, ots, ro, so, ids, E, rows):
     return u8(out), u8(sf)
 
 
-@pytest.mark.parametrize("I", [64, 192, 1536])
+@pytest.mark.parametrize("I", [64, 192, 576, 1536])
 def test_swiglu_quantize_bit_exact(I):
     need_gpu()
     counts = [0, 1, 127, 128, 129, 40]
@@ -54,6 +55,35 @@ def test_swiglu_quantize_bit_exact(I):
     assert np.array_equal(sf, want_sf)
 
 
+@pytest.mark.parametrize("I", [576, 1536])
+def test_swiglu_quantize_y_16_byte_aligned(I):
+    """y starting 16 bytes past a 32-byte boundary (the kernel then reads
+    each lane's 64 bytes as four 16-byte loads) gives the bytes of the
+    32-byte aligned call; both equal the oracle's."""
+    need_gpu()
+    counts = [5, 0, 130, 1, 64]
+    ids = np.array([2, 0, 1, 4, 3], np.int32)
+    ro, ids = groups_from_counts(counts, ids)
+    so = Q.padded_scale_offsets(ro)
+    T, rows = int(ro[-1]), int(so[-1])
+    y = synth.bf16_normal((T, 2 * I), 2.0, seed=I + 5, outlier_p=0.01, outlier_scale=30.0)
+    ots = synth.uniform((5,), 0.001, 0.004, seed=I + 6)
+    base = torch.zeros(T * 2 * I + 64, dtype=torch.bfloat16, device=DEV)
+    off = (-base.data_ptr() // 2) % 16 + 8  # 16 bytes past a 32-byte boundary
+    y_off = base[off:off + T * 2 * I].view(T, 2 * I)
+    y_off.copy_(y.to(DEV))
+    assert y_off.data_ptr() % 32 == 16
+    out_a, sf_a = _run_chained_swiglu(y, ots, ro, so, ids, 5, rows)
+    out_u, sf_u = _run_chained_swiglu(y_off, ots, ro, so, ids, 5, rows)
+    assert np.array_equal(out_a, out_u) and np.array_equal(sf_a, sf_u)
+    want_out, want_sf = S.swiglu_quantize(
+        y.float().numpy(), ots.numpy(), ro, so, ids,
+        out=np.full((T, I // 2), 0xA5, np.uint8),
+        scales=np.full(L.physical_bytes(rows, I // 16), 0x5A, np.uint8), scale_rows_total=rows)
+    assert np.array_equal(out_a, want_out)
+    assert np.array_equal(sf_a, want_sf)
+
+
 def test_swiglu_quantize_full_size_sampled():
     """131072 rows over 128 experts, I = 1536, on sampled rows."""
     need_gpu()
@@ -64,7 +94,8 @@ def test_swiglu_quantize_full_size_sampled():
     y = synth.bf16_normal((T, 2 * I), 3.0, seed=60, device=DEV)
     ots = synth.uniform((128,), 0.002, 0.01, seed=61)
     out, sf = _run_chained_swiglu(y, ots, ro, so, ids, 128, rows)
-    sel = sample_rows(ro, 300, seed=7)
+    # every group: its first, last and middle rows and one row per 128-row block
+    sel = np.concatenate(group_sample_rows(ro))
     grp = np.searchsorted(ro, sel, side="right") - 1
     ysel = y[torch.from_numpy(sel).to(DEV)].float().cpu().numpy()
     lg = L.unswizzle(sf, rows, I // 16)
