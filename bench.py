@@ -518,12 +518,31 @@ def mx_part(d, pk):
         moeq.grouped_matmul_swiglu_mx("mxfp4", c, csf, a, asf, b, bsf, d["es"], d["ro"], d["so"],
                                       d["ids"], I4, K4, rows, d["mt"])
 
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    c2, csf2 = torch.empty_like(c), torch.empty_like(csf)
+
+    def gemm():
+        moeq.grouped_matmul_blockscaled("mxfp4", y, a, asf, b, bsf, d["es"], d["ro"], d["so"],
+                                        d["ids"], N, K4, rows, d["mt"])
+
+    def sw():
+        moeq.swiglu_quantize_mx("mxfp4", c2, csf2, y, d["ro"], d["so"], d["ids"], E4, rows,
+                                d["mt"])
+
     t_q = time_kernel(quant, 10)
     t_f = time_kernel(fused, 10)
+    t_g = time_kernel(gemm, 10)
+    t_s = time_kernel(sw, 10)
     fl = flops_up(d)
+    sw_bytes = y.numel() * 2 + c2.numel() + csf2.numel()
     return {"quantize_mxfp4_ms": round(t_q, 4), "fused_gemm_swiglu_mxfp4_ms": round(t_f, 4),
             "fused_TFLOP/s": round(fl / t_f / 1e9, 1),
             "fused_frac_fp4_peak": round(fl / t_f / 1e9 / (pk["bf16"] * FP4_OVER_BF16), 4),
+            "chained_gemm_bf16_ms": round(t_g, 4),
+            "chained_swiglu_quantize_mxfp4_ms": round(t_s, 4),
+            "chained_swiglu_quantize_mxfp4_GB/s": round(sw_bytes / t_s / 1e6, 1),
+            "chained_swiglu_frac_hbm": round(sw_bytes / t_s / 1e6 / pk["hbm_gbs"], 4),
+            "fused_bytes_equal_chained": bool(torch.equal(c, c2) and torch.equal(csf, csf2)),
             "weights": "bf16 N(0, 0.02) quantized to MXFP4 by the library's grouped quantizer"}
 
 
@@ -548,6 +567,8 @@ def chained_part(d, pk):
     return {"gemm_bf16_ms": round(t_g, 4), "gemm_TFLOP/s": round(fl / t_g / 1e9, 1),
             "swiglu_quantize_ms": round(t_s, 4),
             "swiglu_quantize_GB/s": round((y.numel() * 2 + c.numel() + csf.numel()) / t_s / 1e6, 1),
+            "swiglu_quantize_frac_hbm": round((y.numel() * 2 + c.numel() + csf.numel()) / t_s / 1e6
+                                              / pk["hbm_gbs"], 4),
             "chained_total_ms": round(t_g + t_s, 4), "fused_bytes_equal_chained": same}
 
 

@@ -50,23 +50,15 @@ constexpr int kQWarps = MOEQ_Q_WARPS;
 #ifndef MOEQ_A_MINB
 #define MOEQ_A_MINB 3  // at most 85 registers: 0.161 vs 0.173 ms unbounded (106 registers)
 #endif
-// chained SwiGLU: warps per CTA, 256-h steps in flight, min CTAs per SM.
-// 4-warp CTAs, two steps, at most 48 registers (10 CTAs per SM): 23 % faster
-// than 8-warp CTAs, three steps and 92 registers on 131072 x 3072.
+// chained SwiGLU (NVFP4 and MX outputs): warps per CTA, scale rows per
+// warp, min CTAs per SM (at most 64 registers).  NVFP4 on 131072 x 3072:
+// 0.230 ms with 2 rows per warp, 0.233 ms with 1, 0.234 / 0.238 ms with 4 /
+// 8 (an earlier kernel with 8 (gate, up) pairs per lane and a warp per row:
+// 0.291 ms on the same GPU).
 #ifndef MOEQ_S_WARPS
 #define MOEQ_S_WARPS 4
 #endif
-#ifndef MOEQ_S_U
-#define MOEQ_S_U 2
-#endif
-#ifndef MOEQ_S_MINB
-#define MOEQ_S_MINB 10
-#endif
 constexpr int kSWarps = MOEQ_S_WARPS;
-// chained SwiGLU + NVFP4: scale rows per warp, min CTAs per SM (at most 64
-// registers).  On 131072 x 3072: 0.230 ms with 2 rows per warp, 0.233 ms
-// with 1, 0.234 / 0.238 ms with 4 / 8 (the 8-h-per-lane kernel above:
-// 0.291 ms on the same GPU).
 #ifndef MOEQ_SN_RPW
 #define MOEQ_SN_RPW 2
 #endif
@@ -923,103 +915,142 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_nvfp4_kerne
     }
 }
 
-// Chained SwiGLU + MX requant: one warp per logical scale row; a lane takes
-// 8 (gate, up) pairs = 8 h values per 256-h step, a 32-h block is held by
-// lanes 4i .. 4i+3.  OUT: 1 MXFP4, 2 MXFP8.
-template <int OUT>
-__global__ void __launch_bounds__(kSWarps * 32, MOEQ_S_MINB) swiglu_mx_kernel(SwigluParams p) {
-    static_assert(OUT == 1 || OUT == 2, "MX output formats");
-    pdl_wait();
-    pdl_trigger();
-    __shared__ GroupTable table;
-    const GroupView gv = load_groups(p.g, nullptr, table);
-    const int lane = threadIdx.x & 31;
-    const int64_t prow = (int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5);
-    if (prow >= p.g.scale_rows_total) return;
-    const int gi = scale_row_group(gv, (uint32_t)prow, p.err);
-    if (gi < 0) return;
-    const int64_t kv_atoms = p.I / 128;
-    const uint32_t r0 = gv.ro[gi];
-    const uint32_t rg = gv.ro[gi + 1] - r0;
-    const uint32_t local = (uint32_t)prow - gv.so[gi];
-    if (local >= rg) {
-        if (local < ((rg + 127u) & ~127u) && store_ok(prow < p.g.scale_rows_total, p.err))
-            zero_scale_row(p.scales, prow, kv_atoms, lane);
-        return;
-    }
-    const int64_t row = (int64_t)r0 + local;
-    if (!store_ok(row < p.g.total_rows && prow < p.g.scale_rows_total, p.err)) return;
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.y + row * 2 * p.I);
-    const int64_t nh = p.I;
-    constexpr int U = MOEQ_S_U;  // 256-h steps whose loads are issued together
-    for (int64_t hb = 0; hb < nh; hb += 256 * U) {
-      uint4 v[U][2];
+// SwiGLU + MX requant of one row of y (one warp).  In each 512-h step lane
+// i takes the (gate, up) pairs of h [16 i, 16 i + 16): an MX block of 32 h
+// is held by lanes 2j, 2j + 1.  As in the NVFP4 row, the next step's loads
+// are issued once the current pairs are turned into h.  OUT: 1 MXFP4 (8
+// bytes per lane and step), 2 MXFP8 (16 bytes); the E8M0 scales go to
+// logical scale row prow (one 4-byte word per 8 lanes).
+template <int OUT, bool A32>
+__device__ __forceinline__ void swiglu_mx_row(const uint8_t *src, uint8_t *out_row,
+                                              uint8_t *scales, int64_t prow, int nh,
+                                              int64_t kv_atoms, int lane) {
+    const int nsteps = (nh + 511) >> 9;
+    const int lanes_last = (nh - ((nsteps - 1) << 9)) >> 4;  // nh is a multiple of 128
+    auto load = [&](int s, uint32_t (&d)[16]) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t hl = hb + u * 256 + lane * 8;
-        v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
-        if (hl < nh) {
-            v[u][0] = ld_stream(src + hl / 4);
-            v[u][1] = ld_stream(src + hl / 4 + 1);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t h0 = hb + u * 256;
-        if (h0 >= nh) break;
-        const int64_t hl = h0 + lane * 8;          // first h of this lane
-        const bool active = hl < nh;
-        float h[8];
-        if (active) {
-            const uint4 v0 = v[u][0], v1 = v[u][1];
-            uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {  // (gate, up) pairs, two at a time
-                const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
-                                      bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
-                                      bf16_bits_to_f32(w[i] >> 16), bf16_bits_to_f32(w[i + 1] >> 16));
-                h[i] = f2_lo(hh);
-                h[i + 1] = f2_hi(hh);
-            }
+        for (int i = 0; i < 16; ++i) d[i] = 0u;
+        if (s >= nsteps || (s == nsteps - 1 && lane >= lanes_last)) return;
+        const uint8_t *a = src + ((int64_t)s << 11) + lane * 64;
+        if (A32) {
+            ld_stream32(a, *reinterpret_cast<uint32_t(*)[8]>(&d[0]));
+            ld_stream32(a + 32, *reinterpret_cast<uint32_t(*)[8]>(&d[8]));
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = 0.0f;
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = ld_stream(a + 16 * k);
+                d[4 * k] = v.x;
+                d[4 * k + 1] = v.y;
+                d[4 * k + 2] = v.z;
+                d[4 * k + 3] = v.w;
+            }
         }
+    };
+    uint32_t w[16];
+    load(0, w);
+    const int64_t sf0 = sf_word_offset(prow, 0, kv_atoms);
+    for (int s = 0; s < nsteps; ++s) {
+        const bool active = s < nsteps - 1 || lane < lanes_last;
+        float h[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {  // word i: gate_i in the low half, up_i in the high
+            const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
+                                  bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
+                                  __uint_as_float(w[i] & 0xFFFF0000u),
+                                  __uint_as_float(w[i + 1] & 0xFFFF0000u));
+            h[i] = f2_lo(hh);
+            h[i + 1] = f2_hi(hh);
+        }
+        load(s + 1, w);
         float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(h[i]));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));  // the block's 4 lanes
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(h[i]));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // the block's two lanes
         uint32_t code = 0;
         float f = 0.0f;
         if (m != 0.0f) {
             code = mx_scale_code_f32(m, OUT == 2 ? 8 : 2);
             f = mx_multiplier(code);
         }
-        float q[8];
         const F2 f2v = f2(f, f);
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
+        for (int i = 0; i < 16; i += 2) {
             const F2 t = mul2(f2(h[i], h[i + 1]), f2v);
-            q[i] = f2_lo(t);
-            q[i + 1] = f2_hi(t);
+            h[i] = f2_lo(t);
+            h[i + 1] = f2_hi(t);
         }
-        const uint32_t word = gather4(code, lane, 4);
-        if (active) {
-            if (OUT == 2) {
-                uint2 o = make_uint2(e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16),
-                                     e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16));
-                if (m == 0.0f) o = make_uint2(0u, 0u);  // all-zero block: +0 codes
-                *reinterpret_cast<uint2 *>(p.out + row * p.I + hl) = o;
-            } else {
-                const uint32_t o = m == 0.0f ? 0u : e2m1x8(q);
-                reinterpret_cast<uint32_t *>(p.out + row * (p.I / 2))[hl / 8] = o;
+        // lanes 8j .. 8j+7 hold the scale bytes of one word (two lanes per byte)
+        uint32_t word = code << (8 * ((lane >> 1) & 3));
+        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
+        if (!active) continue;
+        if (OUT == 2) {
+            uint4 o;
+            o.x = e4m3x2(h[0], h[1]) | (e4m3x2(h[2], h[3]) << 16);
+            o.y = e4m3x2(h[4], h[5]) | (e4m3x2(h[6], h[7]) << 16);
+            o.z = e4m3x2(h[8], h[9]) | (e4m3x2(h[10], h[11]) << 16);
+            o.w = e4m3x2(h[12], h[13]) | (e4m3x2(h[14], h[15]) << 16);
+            if (m == 0.0f) o = make_uint4(0u, 0u, 0u, 0u);  // all-zero block: +0 codes
+            reinterpret_cast<uint4 *>(out_row)[s * 32 + lane] = o;
+        } else {
+            float lo8[8], hi8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lo8[i] = h[i];
+                hi8[i] = h[8 + i];
             }
-            if ((lane & 15) == 0)
-                *reinterpret_cast<uint32_t *>(
-                    p.scales + sf_word_offset(prow, hl / 128, kv_atoms)) = word;
+            uint2 o = make_uint2(e2m1x8(lo8), e2m1x8(hi8));
+            if (m == 0.0f) o = make_uint2(0u, 0u);
+            reinterpret_cast<uint2 *>(out_row)[s * 32 + lane] = o;
         }
-      }
+        if ((lane & 7) == 0)
+            *reinterpret_cast<uint32_t *>(scales + sf0 + (int64_t)(s * 4 + (lane >> 3)) * 512) =
+                word;
+    }
+}
+
+// Chained SwiGLU + MX requant (OUT: 1 MXFP4, 2 MXFP8): each warp takes
+// MOEQ_SN_RPW consecutive logical scale rows, looking their group up only
+// when a row leaves the group of the previous one.
+template <int OUT>
+__global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_mx_kernel(SwigluParams p) {
+    static_assert(OUT == 1 || OUT == 2, "MX output formats");
+    pdl_wait();
+    pdl_trigger();
+    __shared__ GroupTable table;
+    const GroupView gv = load_groups(p.g, nullptr, table);
+    const int lane = threadIdx.x & 31;
+    const int64_t kv_atoms = p.I / 128;
+    const int64_t ob = OUT == 2 ? p.I : p.I / 2;  // output bytes per row
+    const bool a32 = (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
+    const int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
+    int gi = -1;
+    uint32_t s0 = 0, s1 = 0, r0 = 0, rg = 0;
+    for (int k = 0; k < MOEQ_SN_RPW; ++k) {
+        const int64_t prow = prow0 + k;  // warp-uniform
+        if (prow >= p.g.scale_rows_total) return;
+        if (gi < 0 || (uint32_t)prow < s0 || (uint32_t)prow >= s1) {
+            gi = scale_row_group(gv, (uint32_t)prow, p.err);
+            if (gi < 0) continue;
+            s0 = gv.so[gi];
+            s1 = gv.so[gi + 1];
+            r0 = gv.ro[gi];
+            rg = gv.ro[gi + 1] - r0;
+        }
+        const uint32_t local = (uint32_t)prow - s0;
+        if (local >= rg) {  // padding row of the group
+            if (local < ((rg + 127u) & ~127u) && store_ok(prow < p.g.scale_rows_total, p.err))
+                zero_scale_row(p.scales, prow, kv_atoms, lane);
+            continue;
+        }
+        const int64_t row = (int64_t)r0 + local;
+        if (!store_ok(row < p.g.total_rows, p.err)) continue;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.y + row * 2 * p.I);
+        uint8_t *out_row = p.out + row * ob;
+        if (a32)
+            swiglu_mx_row<OUT, true>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, lane);
+        else
+            swiglu_mx_row<OUT, false>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, lane);
     }
 }
 
@@ -1141,15 +1172,15 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
                                    uint32_t *err, cudaStream_t s) {
     SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
     if (g.scale_rows_total == 0) return cudaSuccess;
+    const int64_t per_cta = (int64_t)kSWarps * MOEQ_SN_RPW;
     if (out_fmt == 0) {
-        const int64_t per_cta = (int64_t)kSWarps * MOEQ_SN_RPW;
         return launch_pdl(swiglu_nvfp4_kernel,
                           (unsigned)((g.scale_rows_total + per_cta - 1) / per_cta), kSWarps * 32,
                           0, s, p);
     }
-    const int64_t blocks = (g.scale_rows_total + kSWarps - 1) / kSWarps;
-    return launch_pdl(out_fmt == 1 ? swiglu_mx_kernel<1> : swiglu_mx_kernel<2>, (unsigned)blocks,
-                      kSWarps * 32, 0, s, p);
+    return launch_pdl(out_fmt == 1 ? swiglu_mx_kernel<1> : swiglu_mx_kernel<2>,
+                      (unsigned)((g.scale_rows_total + per_cta - 1) / per_cta), kSWarps * 32, 0, s,
+                      p);
 }
 
 }  // namespace moeq

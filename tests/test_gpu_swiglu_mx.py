@@ -38,7 +38,7 @@ def _chained_mx(fmt, y, ro_d, so_d, ids_d, E, rows):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
-@pytest.mark.parametrize("I", [128, 384, 1536])
+@pytest.mark.parametrize("I", [128, 384, 640, 1536])
 def test_swiglu_quantize_mx_bit_exact(fmt, I):
     need_gpu()
     counts = [0, 1, 127, 128, 129, 40]
@@ -62,6 +62,27 @@ def test_swiglu_quantize_mx_bit_exact(fmt, I):
         scales=np.full(L.physical_bytes(rows, I // 32), 0x5A, np.uint8), scale_rows_total=rows)
     assert np.array_equal(u8(out), want_out)
     assert np.array_equal(u8(sf), want_sf)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_swiglu_quantize_mx_y_16_byte_aligned(fmt):
+    """y starting 16 bytes past a 32-byte boundary (16-byte loads) gives the
+    bytes of the 32-byte aligned call."""
+    need_gpu()
+    I = 640
+    ro, ids = groups_from_counts([5, 0, 130, 1, 64], [2, 0, 1, 4, 3])
+    so = Q.padded_scale_offsets(ro)
+    T, rows = int(ro[-1]), int(so[-1])
+    y = synth.bf16_normal((T, 2 * I), 2.0, seed=31, device=DEV)
+    base = torch.zeros(T * 2 * I + 64, dtype=torch.bfloat16, device=DEV)
+    off = (-base.data_ptr() // 2) % 16 + 8  # 16 bytes past a 32-byte boundary
+    y_off = base[off:off + T * 2 * I].view(T, 2 * I)
+    y_off.copy_(y)
+    assert y_off.data_ptr() % 32 == 16
+    ro_d, so_d, ids_d = to_dev_u32(ro), to_dev_u32(so), to_dev_i32(ids)
+    out_a, sf_a = _chained_mx(fmt, y, ro_d, so_d, ids_d, 5, rows)
+    out_u, sf_u = _chained_mx(fmt, y_off, ro_d, so_d, ids_d, 5, rows)
+    assert torch.equal(out_a, out_u) and torch.equal(sf_a, sf_u)
 
 
 def _fused_and_chained_mx(fmt, a, asf, b, bsf, es, ro, so, ids, I, K, rows):
