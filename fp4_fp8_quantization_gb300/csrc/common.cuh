@@ -287,8 +287,8 @@ __device__ __forceinline__ F2 exp_neg2(float x0, float x1) {
     return mul2(p, f2(__int_as_float(s0), __int_as_float(s1)));
 }
 
-// h = silu(g) * u for two (gate, up) pairs.
-__device__ __forceinline__ F2 swiglu2(float g0, float g1, float u0, float u1) {
+// silu(g) = g * sigma(g) for two gates.
+__device__ __forceinline__ F2 silu2(float g0, float g1) {
     const float kSeedA = 1.41176474094390869140625f;      // fp32(24 / 17)
     const float kSeedB = 0.4705882370471954345703125f;    // fp32(8 / 17)
     const F2 e = exp_neg2(-fabsf(g0), -fabsf(g1));
@@ -301,7 +301,50 @@ __device__ __forceinline__ F2 swiglu2(float g0, float g1, float u0, float u1) {
     }
     const F2 er = mul2(e, r);
     const F2 sg = f2(g0 >= 0.0f ? f2_lo(r) : f2_lo(er), g1 >= 0.0f ? f2_hi(r) : f2_hi(er));
-    return mul2(mul2(f2(g0, g1), sg), f2(u0, u1));
+    return mul2(f2(g0, g1), sg);
+}
+
+// h = silu(g) * u for two (gate, up) pairs.
+__device__ __forceinline__ F2 swiglu2(float g0, float g1, float u0, float u1) {
+    return mul2(silu2(g0, g1), f2(u0, u1));
+}
+
+// SiLU of bf16 gates by table.  The table holds silu(g), computed by silu2,
+// for every bf16 g whose biased exponent lies in [kSiluE0, kSiluE0 +
+// kSiluExps), positive gates first, then their negative twins (2 x 4096
+// fp32).  Outside that range the definition reduces exactly (checked for
+// every bf16 value) to silu(g) = g * 1/2 below it (sigma = 1/2 to fp32
+// precision, zero and subnormals included) and to g * (g >= 0 ? 1 : 0)
+// above it (sigma = 1 or 0; inf and NaN as the definition gives them).
+constexpr uint32_t kSiluE0 = 102, kSiluExps = 32;
+constexpr uint32_t kSiluHalf = kSiluExps * 128;           // entries per sign
+constexpr uint32_t kSiluTableBytes = 2 * kSiluHalf * 4;
+
+// Fills the table; every thread of the CTA calls it (a CTA barrier must
+// follow before the table is read).
+__device__ __forceinline__ void build_silu_table(float *tab) {
+    for (uint32_t i = threadIdx.x; i < kSiluHalf; i += blockDim.x) {
+        const uint32_t gb = (kSiluE0 << 7) + i;
+        const F2 sv = silu2(__uint_as_float(gb << 16), __uint_as_float((gb | 0x8000u) << 16));
+        tab[i] = f2_lo(sv);
+        tab[kSiluHalf + i] = f2_hi(sv);
+    }
+}
+
+// silu(g) for the bf16 gate with bits gb (low 16 bits).
+__device__ __forceinline__ float silu_lookup(uint32_t gb, const float *tab) {
+    const uint32_t mag = gb & 0x7FFFu;
+    const uint32_t t = mag - (kSiluE0 << 7);
+    const float g = __uint_as_float(gb << 16);
+    if (t < kSiluHalf) return tab[t + ((gb & 0x8000u) ? kSiluHalf : 0u)];
+    return mag < (kSiluE0 << 7) ? __fmul_rn(g, 0.5f) : __fmul_rn(g, g >= 0.0f ? 1.0f : 0.0f);
+}
+
+// h = silu(g) * u for two (gate, up) words (gate bits in the low half, up
+// in the high half), silu by table.
+__device__ __forceinline__ F2 swiglu2_tab(uint32_t w0, uint32_t w1, const float *tab) {
+    return mul2(f2(silu_lookup(w0 & 0xFFFFu, tab), silu_lookup(w1 & 0xFFFFu, tab)),
+                f2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u)));
 }
 
 // ----------------------------------------------------- tiled scale layout

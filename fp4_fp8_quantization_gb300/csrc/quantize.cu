@@ -50,20 +50,20 @@ constexpr int kQWarps = MOEQ_Q_WARPS;
 #ifndef MOEQ_A_MINB
 #define MOEQ_A_MINB 3  // at most 85 registers: 0.161 vs 0.173 ms unbounded (106 registers)
 #endif
-// chained SwiGLU (NVFP4 and MX outputs): warps per CTA, scale rows per
-// warp, min CTAs per SM (at most 64 registers).  NVFP4 on 131072 x 3072:
-// 0.230 ms with 2 rows per warp, 0.233 ms with 1, 0.234 / 0.238 ms with 4 /
-// 8 (an earlier kernel with 8 (gate, up) pairs per lane and a warp per row:
-// 0.291 ms on the same GPU).
+// chained SwiGLU (NVFP4 and MX outputs): persistent CTAs of kSWarps warps,
+// MOEQ_SN_MINB per SM (each with its SiLU table), MOEQ_SN_RPW consecutive
+// scale rows per warp and turn.  NVFP4 on 131072 x 3072: 0.186 ms with 16
+// warps and 4 rows (0.189 / 0.197 ms with 2 / 8 rows; 32-warp CTAs 0.193
+// ms); the same layout without the table and persistence 0.234 ms.
 #ifndef MOEQ_S_WARPS
-#define MOEQ_S_WARPS 4
+#define MOEQ_S_WARPS 16
 #endif
 constexpr int kSWarps = MOEQ_S_WARPS;
 #ifndef MOEQ_SN_RPW
-#define MOEQ_SN_RPW 2
+#define MOEQ_SN_RPW 4
 #endif
 #ifndef MOEQ_SN_MINB
-#define MOEQ_SN_MINB 8
+#define MOEQ_SN_MINB 2
 #endif
 
 // The group description, read either from a per-CTA shared-memory copy
@@ -795,7 +795,8 @@ template <bool A32>
 __device__ __forceinline__ void swiglu_nvfp4_row(const uint8_t *src, uint8_t *out_row,
                                                  uint8_t *scales, int64_t prow, int nh,
                                                  int64_t kv_atoms, float inv,
-                                                 const float *r_tab, int lane) {
+                                                 const float *r_tab, const float *silu_tab,
+                                                 int lane) {
     const int nsteps = (nh + 511) >> 9;
     const int lanes_last = (nh - ((nsteps - 1) << 9)) >> 4;  // nh is a multiple of 64
     auto load = [&](int s, uint32_t (&d)[16]) {
@@ -826,10 +827,7 @@ __device__ __forceinline__ void swiglu_nvfp4_row(const uint8_t *src, uint8_t *ou
         float h[16];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {  // word i: gate_i in the low half, up_i in the high
-            const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
-                                  bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
-                                  __uint_as_float(w[i] & 0xFFFF0000u),
-                                  __uint_as_float(w[i + 1] & 0xFFFF0000u));
+            const F2 hh = swiglu2_tab(w[i], w[i + 1], silu_tab);
             h[i] = f2_lo(hh);
             h[i + 1] = f2_hi(hh);
         }
@@ -859,26 +857,31 @@ __device__ __forceinline__ void swiglu_nvfp4_row(const uint8_t *src, uint8_t *ou
     }
 }
 
-// Chained SwiGLU + NVFP4: each warp takes MOEQ_SN_RPW consecutive logical
-// scale rows, looking their group up (and building its multiplier table)
-// only when a row leaves the group of the previous one.
+// Chained SwiGLU + NVFP4: persistent CTAs; each builds the SiLU table in
+// dynamic shared memory, then each warp takes MOEQ_SN_RPW consecutive
+// logical scale rows per turn, looking their group up (and building its
+// multiplier table) only when a row leaves the group of the previous one.
 __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_nvfp4_kernel(SwigluParams p) {
     pdl_wait();
     pdl_trigger();
+    extern __shared__ float silu_tab[];
     __shared__ float r_tables[kSWarps][128];
     __shared__ GroupTable table;
-    const GroupView gv = load_groups(p.g, p.out_tensor_scale, table);
+    build_silu_table(silu_tab);
+    const GroupView gv = load_groups(p.g, p.out_tensor_scale, table);  // (CTA barrier)
     const int lane = threadIdx.x & 31;
     float *r_tab = r_tables[threadIdx.x >> 5];
     const int64_t kv_atoms = p.I / 64;
     const bool a32 = (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
-    const int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
     int gi = -1;
     uint32_t s0 = 0, s1 = 0, r0 = 0, rg = 0;
     float inv = 0.0f;
+    const int64_t turn = (int64_t)gridDim.x * kSWarps * MOEQ_SN_RPW;
+    for (int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
+         prow0 < p.g.scale_rows_total; prow0 += turn)
     for (int k = 0; k < MOEQ_SN_RPW; ++k) {
         const int64_t prow = prow0 + k;  // warp-uniform
-        if (prow >= p.g.scale_rows_total) return;
+        if (prow >= p.g.scale_rows_total) break;
         if (gi < 0 || (uint32_t)prow < s0 || (uint32_t)prow >= s1) {
             gi = scale_row_group(gv, (uint32_t)prow, p.err);
             if (gi < 0) continue;
@@ -908,10 +911,10 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_nvfp4_kerne
         uint8_t *out_row = p.out + row * (p.I / 2);
         if (a32)
             swiglu_nvfp4_row<true>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, inv, r_tab,
-                                   lane);
+                                   silu_tab, lane);
         else
             swiglu_nvfp4_row<false>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, inv, r_tab,
-                                    lane);
+                                    silu_tab, lane);
     }
 }
 
@@ -924,7 +927,7 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_nvfp4_kerne
 template <int OUT, bool A32>
 __device__ __forceinline__ void swiglu_mx_row(const uint8_t *src, uint8_t *out_row,
                                               uint8_t *scales, int64_t prow, int nh,
-                                              int64_t kv_atoms, int lane) {
+                                              int64_t kv_atoms, const float *silu_tab, int lane) {
     const int nsteps = (nh + 511) >> 9;
     const int lanes_last = (nh - ((nsteps - 1) << 9)) >> 4;  // nh is a multiple of 128
     auto load = [&](int s, uint32_t (&d)[16]) {
@@ -954,10 +957,7 @@ __device__ __forceinline__ void swiglu_mx_row(const uint8_t *src, uint8_t *out_r
         float h[16];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {  // word i: gate_i in the low half, up_i in the high
-            const F2 hh = swiglu2(bf16_bits_to_f32(w[i] & 0xFFFFu),
-                                  bf16_bits_to_f32(w[i + 1] & 0xFFFFu),
-                                  __uint_as_float(w[i] & 0xFFFF0000u),
-                                  __uint_as_float(w[i + 1] & 0xFFFF0000u));
+            const F2 hh = swiglu2_tab(w[i], w[i + 1], silu_tab);
             h[i] = f2_lo(hh);
             h[i + 1] = f2_hi(hh);
         }
@@ -1009,26 +1009,30 @@ __device__ __forceinline__ void swiglu_mx_row(const uint8_t *src, uint8_t *out_r
     }
 }
 
-// Chained SwiGLU + MX requant (OUT: 1 MXFP4, 2 MXFP8): each warp takes
-// MOEQ_SN_RPW consecutive logical scale rows, looking their group up only
-// when a row leaves the group of the previous one.
+// Chained SwiGLU + MX requant (OUT: 1 MXFP4, 2 MXFP8): persistent CTAs
+// with the SiLU table, MOEQ_SN_RPW consecutive logical scale rows per warp
+// and turn, the group looked up only when a row leaves the previous one's.
 template <int OUT>
 __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_mx_kernel(SwigluParams p) {
     static_assert(OUT == 1 || OUT == 2, "MX output formats");
     pdl_wait();
     pdl_trigger();
+    extern __shared__ float silu_tab[];
     __shared__ GroupTable table;
-    const GroupView gv = load_groups(p.g, nullptr, table);
+    build_silu_table(silu_tab);
+    const GroupView gv = load_groups(p.g, nullptr, table);  // (CTA barrier)
     const int lane = threadIdx.x & 31;
     const int64_t kv_atoms = p.I / 128;
     const int64_t ob = OUT == 2 ? p.I : p.I / 2;  // output bytes per row
     const bool a32 = (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
-    const int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
     int gi = -1;
     uint32_t s0 = 0, s1 = 0, r0 = 0, rg = 0;
+    const int64_t turn = (int64_t)gridDim.x * kSWarps * MOEQ_SN_RPW;
+    for (int64_t prow0 = ((int64_t)blockIdx.x * kSWarps + (threadIdx.x >> 5)) * MOEQ_SN_RPW;
+         prow0 < p.g.scale_rows_total; prow0 += turn)
     for (int k = 0; k < MOEQ_SN_RPW; ++k) {
         const int64_t prow = prow0 + k;  // warp-uniform
-        if (prow >= p.g.scale_rows_total) return;
+        if (prow >= p.g.scale_rows_total) break;
         if (gi < 0 || (uint32_t)prow < s0 || (uint32_t)prow >= s1) {
             gi = scale_row_group(gv, (uint32_t)prow, p.err);
             if (gi < 0) continue;
@@ -1048,9 +1052,11 @@ __global__ void __launch_bounds__(kSWarps * 32, MOEQ_SN_MINB) swiglu_mx_kernel(S
         const uint8_t *src = reinterpret_cast<const uint8_t *>(p.y + row * 2 * p.I);
         uint8_t *out_row = p.out + row * ob;
         if (a32)
-            swiglu_mx_row<OUT, true>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, lane);
+            swiglu_mx_row<OUT, true>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, silu_tab,
+                                     lane);
         else
-            swiglu_mx_row<OUT, false>(src, out_row, p.scales, prow, (int)p.I, kv_atoms, lane);
+            swiglu_mx_row<OUT, false>(src, out_row, p.scales, prow, (int)p.I, kv_atoms,
+                                      silu_tab, lane);
     }
 }
 
@@ -1172,15 +1178,30 @@ cudaError_t launch_swiglu_quantize(int out_fmt, uint8_t *c_q, uint8_t *c_sf, con
                                    uint32_t *err, cudaStream_t s) {
     SwigluParams p{reinterpret_cast<const uint16_t *>(y), I, c_q, c_sf, out_tensor_scale, g, err};
     if (g.scale_rows_total == 0) return cudaSuccess;
+    void (*kern)(SwigluParams) = out_fmt == 0   ? swiglu_nvfp4_kernel
+                                 : out_fmt == 1 ? swiglu_mx_kernel<1>
+                                                : swiglu_mx_kernel<2>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    // per device: the SM count, and the opt-in for the table's dynamic shared
+    // memory (static + dynamic exceed the default 48 KB), set once per kernel
+    static std::atomic<int> sm_cache[kMaxDevices];
+    static std::atomic<int> attr_cache[3][kMaxDevices];
+    const int sms = cached_per_device(sm_cache, dev, [dev]() {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    });
+    const int ok = cached_per_device(attr_cache[out_fmt], dev, [kern]() {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSiluTableBytes) == cudaSuccess ? 1 : 0;
+    });
+    if (!ok) return cudaErrorInvalidValue;
     const int64_t per_cta = (int64_t)kSWarps * MOEQ_SN_RPW;
-    if (out_fmt == 0) {
-        return launch_pdl(swiglu_nvfp4_kernel,
-                          (unsigned)((g.scale_rows_total + per_cta - 1) / per_cta), kSWarps * 32,
-                          0, s, p);
-    }
-    return launch_pdl(out_fmt == 1 ? swiglu_mx_kernel<1> : swiglu_mx_kernel<2>,
-                      (unsigned)((g.scale_rows_total + per_cta - 1) / per_cta), kSWarps * 32, 0, s,
-                      p);
+    const int64_t blocks = std::min<int64_t>((g.scale_rows_total + per_cta - 1) / per_cta,
+                                             (int64_t)sms * MOEQ_SN_MINB);
+    return launch_pdl(kern, (unsigned)blocks, kSWarps * 32, kSiluTableBytes, s, p);
 }
 
 }  // namespace moeq

@@ -135,6 +135,28 @@ def test_silu_every_bf16_input():
     assert np.all(np.abs(got[~big]) <= 1e-30)
 
 
+def test_silu_bf16_tails_reduce_exactly():
+    """The kernels tabulate silu for bf16 gates with biased exponents 102..133
+    and use two closed forms outside that band; every bf16 value (NaN and inf
+    included) must give the definition's bits: g * 1/2 below exponent 102
+    (|g| < 2^-25: e^-|g| rounds to 1, sigma to 1/2) and g * (1 if g >= 0 else
+    0) above exponent 133 (|g| >= 128: e^-|g| is flushed to 0, sigma is 1 or
+    0).  The band's edges are tight: each form fails just inside it."""
+    bits = np.arange(65536, dtype=np.uint32)
+    g = (bits << 16).view(np.float32)
+    expo = (bits >> 7) & 0xFF
+    with np.errstate(all="ignore"):
+        got = S.silu_spec(g).view(np.uint32)
+        tiny = (g * np.float32(0.5)).astype(np.float32).view(np.uint32)
+        large = (g * np.where(g >= 0, np.float32(1.0), np.float32(0.0))).astype(np.float32)
+    large = large.view(np.uint32)
+    below, above = expo < 102, expo > 133
+    assert np.array_equal(got[below], tiny[below])
+    assert np.array_equal(got[above], large[above])
+    assert not np.array_equal(got[expo == 102], tiny[expo == 102])
+    assert not np.array_equal(got[expo == 133], large[expo == 133])
+
+
 def test_swiglu_worked_blocks():
     for name, attrs, _, body in cases("swiglu_blocks.txt", 4):
         gate = np.array(body[0].split(), np.float32)
