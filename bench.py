@@ -49,6 +49,21 @@ NOMINAL = {"hbm_gbs": 7900.0, "fp8_tflops": 4500.0, "fp4_tflops": 13500.0}
 # 128 SM cycles for every kind, so FP4 (K = 64) does 2 * 128 * 256 * 64 / 128
 # = 32768 flop per SM cycle (FP8 half, bf16 a quarter).
 FP4_FLOP_PER_SM_CYCLE = 32768
+# The NVFP4 GEMMs run 256-row x 256-column tiles over CTA pairs: each
+# expert's rows are padded to whole 256-row pair tiles, the persistent pairs
+# take tiles t, t + pairs, ...; every tile issues K / 64 pair MMAs of 128
+# cycles.
+FP4_PAIR_TILE_M, FP4_PAIR_TILE_N, FP4_MMA_K, FP4_MMA_CYCLES = 256, 256, 64, 128
+
+
+def fp4_schedule_floor(counts, N, K, sms, sm_mhz):
+    """MMA time (ms) of the fused GEMM's own schedule at the measured MMA
+    rate, with the pair tiles it runs in all and on its busiest pair."""
+    tiles = sum(-(-int(c) // FP4_PAIR_TILE_M) for c in counts if c) * -(-N // FP4_PAIR_TILE_N)
+    pairs = sms // 2
+    per_pair = -(-tiles // pairs)
+    cycles = per_pair * (K // FP4_MMA_K) * FP4_MMA_CYCLES
+    return cycles / (sm_mhz * 1e3), tiles, per_pair
 # The fused GEMM's DRAM traffic comes from a committed ncu summary that names
 # the sha256 of the kernel sources it was captured with; a changed kernel
 # makes the figure stale and the bench reports null.
@@ -860,8 +875,9 @@ def run_moeq(args, rank, world):
     achieved = fl / (t_f * 1e-3) / 1e12
     traffic, traffic_note = fused_traffic_bytes()
     sm_mhz = clk.get("sm_mhz") or 2070.0
-    mma_ceiling = FP4_FLOP_PER_SM_CYCLE * torch.cuda.get_device_properties(0).multi_processor_count \
-        * sm_mhz * 1e6 / 1e12
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mma_ceiling = FP4_FLOP_PER_SM_CYCLE * sms * sm_mhz * 1e6 / 1e12
+    floor_ms, floor_tiles, floor_per_pair = fp4_schedule_floor(d["counts"], d["N"], K4, sms, sm_mhz)
     roof = {"kernel": "grouped_gemm_kernel<NVFP4, fused SwiGLU>", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / fp4_peak, 4), "traffic": traffic,
@@ -873,6 +889,14 @@ def run_moeq(args, rank, world):
             "mma_ceiling_note": "measured tcgen05 FP4 rate of this part (32768 flop per SM cycle: "
                                 "one M128xN256xK64 MMA per 128 cycles, 2x FP8, 4x bf16) x SMs x the "
                                 "run's median SM clock",
+            "mma_schedule_floor_ms": round(floor_ms, 4),
+            "frac_mma_schedule_floor": round(floor_ms / t_f, 4),
+            "mma_schedule_floor_note": (
+                f"MMA time of the kernel's own schedule at that rate: expert rows padded to "
+                f"256-row CTA-pair tiles, {floor_tiles} pair tiles of 256x256 "
+                f"({fl / (2 * FP4_PAIR_TILE_M * FP4_PAIR_TILE_N * K4):.0f} without padding), "
+                f"{floor_per_pair} on the busiest of {sms // 2} pairs, K/64 MMAs of 128 cycles "
+                f"each"),
             "algorithmic_flops_per_launch": fl}
     breakdown = {"offsets_amax_ms": round(t_pre, 4), "quantize_nvfp4_ms": round(t_q, 4),
                  "fused_gemm_swiglu_ms": round(t_f, 4)}

@@ -234,7 +234,9 @@ def run_blockscaled(fmt, a, asf, b, bsf, es, ro, so, ids, N, K, rows):
 
 @pytest.mark.parametrize("fmt,es_on", [("nvfp4", True), ("mxfp8", False), ("mxfp8", True),
                                        ("mxfp4", False), ("mxfp4", True)])
-@pytest.mark.parametrize("N,K", [(256, 512), (128, 1024), (512, 1536)])
+# N = 384 and 1152: with the FP4 kinds' 256-column tiles the last n-tile lies
+# half past N
+@pytest.mark.parametrize("N,K", [(256, 512), (128, 1024), (512, 1536), (384, 512), (1152, 256)])
 def test_blockscaled_ragged_multitile(fmt, es_on, N, K):
     need_gpu()
     from oracle import quantize as Q
