@@ -100,3 +100,42 @@ def test_blockscaled_copies_and_stores_in_bounds(kind, sf_vec, elem_bits, pair):
             total += _check(counts, N, 4096, sf_vec, elem_bits, pair,
                             bn=128 if kind == "mxfp8" else 256)
     assert total > 1000
+
+
+def _staged_offset(row, piece):
+    """Byte offset of 16-byte piece `piece` of row `row` in an epilogue warp's
+    2 KB bf16 staging buffer: 64-byte rows, pieces XOR-swizzled by row pair."""
+    return row * 64 + ((piece ^ ((row >> 1) & 3)) << 4)
+
+
+@pytest.mark.parametrize("nvalid", [0, 1, 7, 8, 31, 32])
+def test_staged_bf16_chunk_stores(nvalid):
+    """The bf16 epilogue's staged stores of one 32 x 32 chunk: thread t
+    writes its row t's four pieces, then in each of 4 rounds lane l reads
+    row (l >> 2) + 8 i, piece l & 3 and stores it if the row is among the
+    warp's first nvalid.  Every (valid row, piece) is stored exactly once, no
+    other row, all offsets in the buffer, and each 8-lane phase of both
+    passes touches 8 distinct groups of 4 banks (no bank conflict)."""
+    stored = {}
+    for i in range(4):
+        for lane in range(32):
+            row, piece = (lane >> 2) + 8 * i, lane & 3
+            off = _staged_offset(row, piece)
+            assert 0 <= off and off + 16 <= 2048
+            if row < nvalid:
+                stored[(row, piece)] = stored.get((row, piece), 0) + 1
+    assert stored == {(r, k): 1 for r in range(nvalid) for k in range(4)}
+    # the write pass: thread t stores piece j of its own row t
+    for j in range(4):
+        for phase in range(4):
+            banks = {(_staged_offset(t, j) // 16) % 8 for t in range(8 * phase, 8 * phase + 8)}
+            assert len(banks) == 8
+    # the read pass
+    for i in range(4):
+        for phase in range(4):
+            lanes = range(8 * phase, 8 * phase + 8)
+            banks = {(_staged_offset((l >> 2) + 8 * i, l & 3) // 16) % 8 for l in lanes}
+            assert len(banks) == 8
+    # each written row's pieces are distinct 16-byte slots of that row
+    for r in range(32):
+        assert sorted(_staged_offset(r, k) - r * 64 for k in range(4)) == [0, 16, 32, 48]
