@@ -61,7 +61,7 @@ enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2, kMxfp4 = 3 };
 enum Epi { kBf16 = 0, kSwiglu = 1, kSwigluMx = 2 };
 
 template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
-          int PAIR_, int SF_LOADER_ = 1, bool STAGED_ = true>
+          int PAIR_, int SF_LOADER_ = 1>
 struct Cfg {
     static constexpr int BM = 128;                              // rows of A per CTA
     static constexpr int PAIR = PAIR_;                          // CTAs per MMA (cta_group)
@@ -107,11 +107,11 @@ struct Cfg {
     static constexpr int SF_COLS_STAGE = SF_COLS_A + SF_COLS_B;
     static constexpr int TMEM_COLS = 512;
     // bf16 out: a 2 KB staging buffer per epilogue warp (one 32 x 32 chunk of
-    // its rows) after the stages, for coalesced stores, when STAGED_ and
-    // where it fits (else each thread stores its own row)
+    // its rows) after the stages, for coalesced stores, where it fits (else
+    // each thread stores its own row)
     static constexpr bool EPI_BUF_FITS =
         STAGES * STAGE_BYTES + EPI_WARPS * 2048 + 1024 <= 222 * 1024;
-    static constexpr int EPI_BUF_BYTES = (EPI == kBf16 && EPI_BUF_FITS && STAGED_) ? 2048 : 0;
+    static constexpr int EPI_BUF_BYTES = (EPI == kBf16 && EPI_BUF_FITS) ? 2048 : 0;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + 1024;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 222 * 1024, "dynamic shared memory beside the static part");
@@ -196,6 +196,25 @@ __device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y,
                  : "memory");
 }
 
+// TMA tensor store of a shared-memory box (bulk async-group of this thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     map),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the thread's bulk stores have read their shared memory / have completed
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -208,12 +227,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
 // Epilogue of one 32-column accumulator chunk of this thread's row.
 //   bf16 out: c[row, n] = bf16(acc * scale(s)); FP8 rowwise applies
 //             a_scale (rs) then b_scale[e, n]; block-scaled the expert scale.
-//             With a staging buffer, the warp's 32 x 32 chunk goes through it
-//             (sbuf, a shared address; 64-byte rows whose 16-byte pieces are
-//             XOR-swizzled by row pair, so both passes are free of bank
-//             conflicts) and is stored with four lanes per row, 8 rows of 64
-//             contiguous bytes per instruction; the warp's first nvalid rows
-//             are written.  Without one, each valid thread stores its row.
+//             With a staging buffer, the warp's 32 x 32 chunk is written into
+//             it (sbuf, a shared address; 64-byte rows whose 16-byte pieces
+//             are XOR-swizzled by row pair: the tensor map's 64-byte swizzle,
+//             free of bank conflicts) and leaves as one tensor store (tmc)
+//             when all 32 rows lie in the group; otherwise it is read back
+//             transposed and stored with four lanes per row, 8 rows of 64
+//             contiguous bytes per instruction, the warp's first nvalid rows
+//             only.  Without a buffer, each valid thread stores its row.
 //   SwiGLU:   16 (gate, up) pairs -> 16 h -> one NVFP4 block; returns the
 //             E4M3 scale code, writes the 8 packed bytes.  gate and up are
 //             bf16((acc * s) * rsr): s the expert scale, rsr the row scale
@@ -222,7 +243,8 @@ template <class C, int KIND, int EPI>
 __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32_t (&r)[32],
                                                    int nc, int e, int64_t row, bool valid,
                                                    float rs, float inv_out, float rsr = 1.0f,
-                                                   uint32_t sbuf = 0, int nvalid = 0) {
+                                                   uint32_t sbuf = 0, int nvalid = 0,
+                                                   const CUtensorMap *tmc = nullptr) {
     if (EPI == kBf16) {
         const int lane = threadIdx.x & 31;
         uint32_t w[16];
@@ -267,11 +289,26 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
             }
             return 0u;
         }
-        __syncwarp();  // the previous chunk's reads of the buffer are done
+        // the previous chunk's reads of the buffer are done (the lanes' and
+        // the tensor store's)
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             st_shared_v4(sbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), w[j * 4],
                          w[j * 4 + 1], w[j * 4 + 2], w[j * 4 + 3]);
+        if (nvalid == 32) {
+            // a whole 32-row chunk: one tensor store (the buffer's layout is
+            // the 64-byte swizzle of the tensor map; columns past N and rows
+            // past the output are clipped by the copy)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmc, sbuf, nc, (int)(row - lane));
+                bulk_commit();
+            }
+            return 0u;
+        }
         __syncwarp();
         const int k = lane & 3;
         const int n = nc + k * 8;
@@ -454,7 +491,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA,
-                        const __grid_constant__ CUtensorMap tmSFB, const Params p) {
+                        const __grid_constant__ CUtensorMap tmSFB,
+                        const __grid_constant__ CUtensorMap tmC, const Params p) {
     constexpr bool PAIRED = C::PAIR > 1;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[C::STAGES];
@@ -834,7 +872,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
                         sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
                                                                 valid, rs, inv_out, rsr, sbuf,
-                                                                nvalid)
+                                                                nvalid, &tmC)
                                    << (8 * ch);
                 }
             } else {
@@ -849,7 +887,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (lane == 0) release(buf);
                     }
                     epilogue_chunk<C, KIND, EPI>(p, r, ncol0 + ch * 32, e, row, valid, rs,
-                                                 inv_out, 1.0f, sbuf, nvalid);
+                                                 inv_out, 1.0f, sbuf, nvalid, &tmC);
                 }
             }
             if (EPI == kSwiglu && mb_in_group) {
@@ -858,6 +896,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                valid ? sfbytes : 0u, nblk);
             }
         }
+        // this warp's tensor stores have completed
+        if (C::EPI_BUF_BYTES && lane == 0) bulk_wait_all();
     }
 
     // this CTA's loads, MMAs and stores are all issued: the next kernel's
@@ -1007,15 +1047,16 @@ int sm_count() {
 }
 
 template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1,
-          int PAIR = 1, bool STAGED = true>
+          int PAIR = 1>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, PAIR, MOEQ_SF_LOADER, STAGED>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, PAIR, MOEQ_SF_LOADER>;
     const int64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
-    CUtensorMap tA, tB, tSFA, tSFB;
+    CUtensorMap tA, tB, tSFA, tSFB, tC;
     memset(&tSFA, 0, sizeof(tSFA));
     memset(&tSFB, 0, sizeof(tSFB));
+    memset(&tC, 0, sizeof(tC));
     cuuint64_t da[2] = {(cuuint64_t)kbytes, (cuuint64_t)T};
     cuuint64_t sa[1] = {(cuuint64_t)kbytes};
     cuuint64_t db[3] = {(cuuint64_t)kbytes, (cuuint64_t)a.N, (cuuint64_t)E};
@@ -1030,6 +1071,20 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
         if (!make_sfb_map(&tSFB, a.b_sf, E * ((a.N + 127) / 128), kv_atoms, 2 * C::SF_ATOMS, C::RB))
             return cudaErrorInvalidValue;
         (void)sfb_bytes;
+    }
+    if (C::EPI_BUF_BYTES) {
+        // bf16 output [T, N], boxes of 32 rows x 32 columns (64 bytes) in
+        // the staging buffer's 64-byte swizzle
+        EncodeTiledFn enc = encode_fn();
+        if (!enc) return cudaErrorInvalidValue;
+        cuuint64_t dc[2] = {(cuuint64_t)a.N, (cuuint64_t)T};
+        cuuint64_t sc[1] = {(cuuint64_t)a.N * 2};
+        cuuint32_t bc[2] = {32, 32};
+        cuuint32_t ec[2] = {1, 1};
+        if (enc(&tC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.c, dc, sc, bc, ec,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     Params p;
     p.a_offsets = a.groups.row_offsets;
@@ -1073,7 +1128,7 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     if (attr_err != cudaSuccess) return attr_err;
     if (PAIR == 1) {
         const int grid = (int)(tiles_ub < sm_count() ? (tiles_ub > 0 ? tiles_ub : 1) : sm_count());
-        return launch_pdl(kern, grid, C::THREADS, C::SMEM_BYTES, s, tA, tB, tSFA, tSFB, p);
+        return launch_pdl(kern, grid, C::THREADS, C::SMEM_BYTES, s, tA, tB, tSFA, tSFB, tC, p);
     }
     // persistent CTA pairs (clusters of two): as many as can be resident
     cudaLaunchConfig_t cfg = {};
@@ -1101,7 +1156,7 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     int64_t clusters = tiles_ub < max_clusters ? (tiles_ub > 0 ? tiles_ub : 1) : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * PAIR), 1, 1);
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSFA, tSFB, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSFA, tSFB, tC, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1183,20 +1238,9 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
                 a, s);
         return run_gemm<kFp8Rowwise, kBf16, 64, 8, 2, 4>(a, s);
     }
-    // FP4 bf16 out: stores staged through shared memory when a tile's
-    // mainloop is short (K <= 2048: at most 8 k-steps of 256), where the
-    // epilogue's stores bound the kernel (NVFP4 K 1536, N 4096 on the
-    // 128-expert rows: 0.446 against 0.531 ms); direct stores for longer K,
-    // where the staging's extra instructions cost more (K 4096: 0.688
-    // against 0.662 ms)
-    const bool staged = a.K <= 2048;
-    if (a.kind == kNvfp4 && a.epi == kBf16) {
-        if (staged)
-            return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
-                            MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS, P, true>(a, s);
+    if (a.kind == kNvfp4 && a.epi == kBf16)
         return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
-                        MOEQ_SF_WARPS, P, false>(a, s);
-    }
+                        MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
                         MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
@@ -1205,13 +1249,9 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
                         MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp8 && a.epi == kSwigluMx)
         return run_gemm<kMxfp8, kSwigluMx, 128, MOEQ_MX8_STAGES, 2, 8>(a, s);
-    if (a.kind == kMxfp4 && a.epi == kBf16) {
-        if (staged)
-            return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
-                            MOEQ_FP4_EPI_WARPS, MOEQ_SF_WARPS, P, true>(a, s);
+    if (a.kind == kMxfp4 && a.epi == kBf16)
         return run_gemm<kMxfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
-                        MOEQ_SF_WARPS, P, false>(a, s);
-    }
+                        MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp8 && a.epi == kBf16)
         return run_gemm<kMxfp8, kBf16, 128, MOEQ_MX8_STAGES, 2, 4>(a, s);
     return cudaErrorNotSupported;
