@@ -289,6 +289,7 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
             }
             return 0u;
         }
+        if (nc >= p.N) return 0u;  // a chunk past N (N a multiple of 16, not of 32)
         // the previous chunk's reads of the buffer are done (the lanes' and
         // the tensor store's)
         if (lane == 0) bulk_wait_read_all();
