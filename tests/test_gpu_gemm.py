@@ -314,6 +314,25 @@ def test_nvfp4_blockscaled_moe_scale_sampled():
                                ro, so, ids, N, K, 256)
 
 
+def test_nvfp4_down_projection_shape_sampled():
+    """The MoE layer's down-projection: 128 experts, 16384 tokens top-8 ->
+    131072 rows, K = 1536, N = 4096 (a short mainloop, so the bf16 epilogue's
+    staged tensor stores and the lanes' masked stores of chunks that reach
+    past a group's end carry most of the output): every group on rows of its
+    first, middle and last m-block."""
+    need_gpu()
+    counts, ro, ids, so = _cfg4_groups(seed=2)
+    T, E, N, K = int(ro[-1]), 128, 4096, 1536
+    rows = int(so[-1])
+    a, asf, b, bsf, es = blockscaled_inputs("nvfp4", T, E, N, K, rows, seed=60, device=DEV)
+    c = run_blockscaled("nvfp4", a, asf, b, bsf, es, ro, so, ids, N, K, rows)
+    # every row lies in a group: no element keeps the canary the output was
+    # filled with (outputs here are of order 1e2, never exactly -12288)
+    assert not bool(torch.any(c == CANARY))
+    _check_blockscaled_sampled("nvfp4", c, a, u8(asf), b, u8(bsf), es.cpu().numpy(),
+                               ro, so, ids, N, K, 256)
+
+
 def test_mxfp8_decode_shape_sampled():
     """256 experts, 64 tokens top-8 -> 512 rows, K = 7168, N = 4096, MXFP8:
     every group, all its rows."""
