@@ -29,6 +29,12 @@ def _rowwise_inputs(T, E, N, K, seed, a_std=1.0, b_std=0.5, device="cpu"):
     return a, b, sa, sb
 
 
+def _assert_all_written(c):
+    """Every row of these outputs lies in a group: no element may keep the
+    canary the buffer was filled with (their outputs are far from -12288)."""
+    assert not bool(torch.any(c == CANARY))
+
+
 def _run_rowwise(a, b, sa, sb, ro, ids, T=None):
     T = a.shape[0] if T is None else T
     c = torch.full((T, b.shape[1]), CANARY, dtype=torch.bfloat16, device=DEV)
@@ -153,10 +159,11 @@ def test_rowwise_fp8_moe_scale_sampled():
     T, E, N, K = int(ro[-1]), 64, 4096, 7168
     a, sa = synth.fp8_rowwise((T, K), 1.0, seed=10, device=DEV)
     b, sb = synth.fp8_rowwise((E, N, K), 0.02, seed=11, device=DEV)
-    c = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    c = torch.full((T, N), CANARY, dtype=torch.bfloat16, device=DEV)
     moeq.grouped_matmul_rowwise_fp8(c, a, b, sa, sb.reshape(E, N), to_dev_u32(ro),
                                     to_dev_i32(ids), max_tokens_per_expert=int(counts.max()))
     torch.cuda.synchronize()
+    _assert_all_written(c)
     _check_rowwise_sampled(c, a, sa, b, sb.reshape(E, N), ro, ids, N, 256)
 
 
@@ -169,10 +176,11 @@ def test_rowwise_fp8_decode_shape_sampled():
     T, E, N, K = int(ro[-1]), 256, 4096, 7168
     a, sa = synth.fp8_rowwise((T, K), 1.0, seed=20, device=DEV)
     b, sb = synth.fp8_rowwise((E, N, K), 0.02, seed=21, device=DEV)
-    c = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    c = torch.full((T, N), CANARY, dtype=torch.bfloat16, device=DEV)
     moeq.grouped_matmul_rowwise_fp8(c, a, b, sa, sb.reshape(E, N), to_dev_u32(ro),
                                     to_dev_i32(ids), max_tokens_per_expert=int(counts.max()))
     torch.cuda.synchronize()
+    _assert_all_written(c)
     _check_rowwise_sampled(c, a, sa, b, sb.reshape(E, N), ro, ids, N, 256, all_rows=True)
 
 
@@ -310,6 +318,7 @@ def test_nvfp4_blockscaled_moe_scale_sampled():
     rows = int(so[-1])
     a, asf, b, bsf, es = blockscaled_inputs("nvfp4", T, E, N, K, rows, seed=40, device=DEV)
     c = run_blockscaled("nvfp4", a, asf, b, bsf, es, ro, so, ids, N, K, rows)
+    _assert_all_written(c)
     _check_blockscaled_sampled("nvfp4", c, a, u8(asf), b, u8(bsf), es.cpu().numpy(),
                                ro, so, ids, N, K, 256)
 
@@ -326,9 +335,7 @@ def test_nvfp4_down_projection_shape_sampled():
     rows = int(so[-1])
     a, asf, b, bsf, es = blockscaled_inputs("nvfp4", T, E, N, K, rows, seed=60, device=DEV)
     c = run_blockscaled("nvfp4", a, asf, b, bsf, es, ro, so, ids, N, K, rows)
-    # every row lies in a group: no element keeps the canary the output was
-    # filled with (outputs here are of order 1e2, never exactly -12288)
-    assert not bool(torch.any(c == CANARY))
+    _assert_all_written(c)
     _check_blockscaled_sampled("nvfp4", c, a, u8(asf), b, u8(bsf), es.cpu().numpy(),
                                ro, so, ids, N, K, 256)
 
@@ -345,6 +352,7 @@ def test_mxfp8_decode_shape_sampled():
     rows = int(so[-1])
     a, asf, b, bsf, _ = blockscaled_inputs("mxfp8", T, E, N, K, rows, seed=50, device=DEV)
     c = run_blockscaled("mxfp8", a, asf, b, bsf, None, ro, so, ids, N, K, rows)
+    _assert_all_written(c)
     _check_blockscaled_sampled("mxfp8", c, a, u8(asf), b, u8(bsf), None, ro, so, ids,
                                N, K, 128, all_rows=True)
 
@@ -358,6 +366,7 @@ def test_mxfp4_blockscaled_moe_scale_sampled():
     rows = int(so[-1])
     a, asf, b, bsf, _ = blockscaled_inputs("mxfp4", T, E, N, K, rows, seed=45, device=DEV)
     c = run_blockscaled("mxfp4", a, asf, b, bsf, None, ro, so, ids, N, K, rows)
+    _assert_all_written(c)
     _check_blockscaled_sampled("mxfp4", c, a, u8(asf), b, u8(bsf), None, ro, so, ids,
                                N, K, 256)
 
