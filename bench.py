@@ -119,8 +119,8 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--log", default=os.environ.get("MOEQ_METRICS_LOG"),
                    help="also append the JSON line to this file (default: $MOEQ_METRICS_LOG)")
-    p.add_argument("--profile", choices=["fused", "quantize", "fp8", "decode_fp8", "chained",
-                                          "swiglu", "dispatch"],
+    p.add_argument("--profile", choices=["fused", "fused_mx", "quantize", "fp8", "decode_fp8",
+                                          "chained", "swiglu", "dispatch"],
                    help="run only --warmup + --steps launches of one kernel on a small case "
                         "(inputs larger than L2, under 1 GB) for a profiler; no JSON line")
     return p.parse_args()
@@ -981,7 +981,7 @@ def run_profile_case(args):
                              torch.empty(n, **i32), torch.empty(E4 + 1, **i32))
         dst = torch.empty(n, **i32)
         fn = lambda: moeq.dispatch_mxfp4(tok, tk, q, sf, ro, eids, src, so, dst_info=dst)
-    elif args.profile in ("fused", "chained", "quantize", "swiglu"):
+    elif args.profile in ("fused", "fused_mx", "chained", "quantize", "swiglu"):
         # 32 experts, 4096 tokens top-8 -> 32768 rows, K 4096, I 1536
         counts = synth.routing_counts(4096, 8, 32, seed=0)
         ro, ids = synth.ragged_groups(counts)
@@ -1003,6 +1003,18 @@ def run_profile_case(args):
             q = torch.empty((T, K4 // 2), dtype=torch.uint8, device=dev)
             sf = torch.empty(moeq.sf_bytes(rows, K4 // 16), dtype=torch.uint8, device=dev)
             fn = lambda: moeq.grouped_quantize("nvfp4", x, q, sf, ro_d, so_d, ids_d, ts, 8, rows)
+        elif args.profile == "fused_mx":
+            # the fused MXFP4 GEMM + SwiGLU + MXFP4 requant on the same shapes
+            a = synth.random_fp4_packed((T, K4 // 2), seed=1, device=dev)
+            asf = synth.random_bytes(moeq.sf_bytes(rows, K4 // 32), 118, 130, seed=2, device=dev)
+            b = synth.random_fp4_packed((32, N, K4 // 2), seed=3, device=dev)
+            bsf = synth.random_bytes(32 * moeq.sf_bytes(N, K4 // 32), 116, 126, seed=4,
+                                     device=dev)
+            es = synth.uniform((32,), 0.5, 2.0, seed=5, device=dev)
+            c = torch.empty((T, I4 // 2), dtype=torch.uint8, device=dev)
+            csf = torch.empty(moeq.sf_bytes(rows, I4 // 32), dtype=torch.uint8, device=dev)
+            fn = lambda: moeq.grouped_matmul_swiglu_mx("mxfp4", c, csf, a, asf, b, bsf, es, ro_d,
+                                                       so_d, ids_d, I4, K4, rows)
         else:
             a = synth.random_fp4_packed((T, K4 // 2), seed=1, device=dev)
             asf = synth.random_bytes(moeq.sf_bytes(rows, K4 // 16), 0x20, 0x30, seed=2, device=dev)
