@@ -100,6 +100,16 @@ struct Cfg {
     static constexpr int SF_WARP0 = 2 + SF_LOADER;
     static constexpr int EPI_WARP0 = SF_WARP0 + SF_WARPS;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    // fused SwiGLU epilogues on CTA pairs: the control warpgroup (producer,
+    // MMA and scale-copy warps) gives registers to the epilogue warpgroups,
+    // whose SiLU evaluations otherwise spill (setmaxnreg acts per warpgroup
+    // and redistributes exactly the registers the block is launched with;
+    // the host checks the compiled count before launching)
+    static constexpr bool NREG = EPI != kBf16 && PAIR_ == 2 && EPI_WARP0 == 4 && THREADS == 384;
+    static constexpr int LAUNCH_REGS = 65536 / THREADS / 8 * 8;
+    static constexpr int NREG_CTRL = 104;
+    static constexpr int NREG_EPI =
+        NREG ? (THREADS * LAUNCH_REGS - 32 * EPI_WARP0 * NREG_CTRL) / (32 * EPI_WARPS) / 8 * 8 : 0;
     static constexpr int ACC_COLS = BN;
     static constexpr int SF_COLS_A = SF_ATOMS * 4;
     static constexpr int SF_COLS_B = SF_ATOMS * 4 * RB;
@@ -114,6 +124,10 @@ struct Cfg {
     static constexpr int EPI_BUF_BYTES = (EPI == kBf16 && EPI_BUF_FITS) ? 2048 : 0;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + 1024;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(!NREG || (NREG_EPI >= LAUNCH_REGS && NREG_EPI <= 256 &&
+                            32 * EPI_WARP0 * NREG_CTRL + 32 * EPI_WARPS * NREG_EPI <=
+                                THREADS * LAUNCH_REGS),
+                  "register split by warpgroups");
     static_assert(SMEM_BYTES <= 222 * 1024, "dynamic shared memory beside the static part");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
@@ -588,6 +602,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t rank = PAIRED ? cluster_ctarank() : 0u;   // m-block within the pair
     const uint32_t cid = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
 
+    if (warp < C::EPI_WARP0) {
+    if constexpr (C::NREG) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::NREG_CTRL));
     if (warp == 0 || (C::SF_LOADER && warp == 2)) {
         // ------------------------------------------------ TMA producers
         // Warp 0 loads the A and B tiles, warp 2 (or warp 0 as well, without
@@ -794,7 +810,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tc_commit<C::PAIR>(&sf_drain_bar);
             mbar_drain(&sf_drain_bar, 0);
         }
-    } else if (warp >= C::EPI_WARP0) {
+    }
+    } else {
+    if constexpr (C::NREG) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::NREG_EPI));
+    {
         // ------------------------------------------------ epilogue
         const int quad = warp & 3;
         const int cgrp = (warp - C::EPI_WARP0) >> 2;  // column group of this warp
@@ -899,6 +918,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         // this warp's tensor stores have completed
         if (C::EPI_BUF_BYTES && lane == 0) bulk_wait_all();
+    }
     }
 
     // this CTA's loads, MMAs and stores are all issued: the next kernel's
@@ -1124,6 +1144,14 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
     cached_per_device(attr_done, dev, [&]() {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::SMEM_BYTES);
+        if (attr_err == cudaSuccess && C::NREG) {
+            // the register split assumes the block holds THREADS x
+            // LAUNCH_REGS registers: refuse to launch a build that differs
+            cudaFuncAttributes fa;
+            attr_err = cudaFuncGetAttributes(&fa, kern);
+            if (attr_err == cudaSuccess && fa.numRegs != C::LAUNCH_REGS)
+                attr_err = cudaErrorInvalidConfiguration;
+        }
         return attr_err == cudaSuccess ? 1 : 0;
     });
     if (attr_err != cudaSuccess) return attr_err;
