@@ -735,7 +735,9 @@ def run_e2e(d, args, world, fl, form):
     form "rows": H2D of the 131072 gathered rows + group offsets,
     up_projection_step."""
     from fp4_fp8_quantization_gb300 import moeq, synth
-    n_copy = 4
+    # host-to-device copy streams (one: 0.972 against 0.990 ms per step with
+    # the copy split over four)
+    n_copy = int(os.environ.get("MOEQ_E2E_COPY_STREAMS", "1"))
     if form == "tokens":
         host = {"tok": synth.bf16_normal((TOK4, K4), 1.0, seed=80).pin_memory(),
                 "tk": torch.from_numpy(synth.topk_ids(TOK4, TOPK4, E4, seed=0)).pin_memory()}
@@ -844,7 +846,8 @@ def run_e2e(d, args, world, fl, form):
                      "routing and NVFP4 quantization of the routed rows on the GPU"
                      if form == "tokens" else
                      "131072 pre-gathered bf16 rows x 4096 + group offsets"),
-           "pipelining": f"H2D of step i+1 on {n_copy} copy streams overlaps compute of step i",
+           "pipelining": (f"H2D of step i+1 on {n_copy} copy stream(s) and D2H of step i-1 "
+                          f"overlap the compute of step i"),
            "single_copy_h2d_GB/s": round(big / h0.elapsed_time(h1) / 1e6, 1)}
     # the same compute without the copies, device time (CUDA events)
     dev_ms = time_kernel(lambda: compute(bufs[0]), steps)
