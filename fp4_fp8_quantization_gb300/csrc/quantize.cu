@@ -39,10 +39,15 @@ namespace {
 #define MOEQ_Q_MINB 8
 #endif
 constexpr int kQWarps = MOEQ_Q_WARPS;
-// amax pass: warps per CTA, rows per warp on large inputs (>= 65536 rows:
-// 2 is 2 % faster than 4 on 131072 x 4096), min CTAs per SM
+// amax pass: warps per CTA on large inputs (>= 65536 rows) and on smaller
+// ones (8192 x 4096: 14.3 us with 4-warp CTAs against 15.1 with 8; 131072 x
+// 4096: 154 us with 8 against 164 with 4), rows per warp on large inputs
+// (2 is 2 % faster than 4 on 131072 x 4096), min CTAs per SM
 #ifndef MOEQ_A_WARPS
 #define MOEQ_A_WARPS 8
+#endif
+#ifndef MOEQ_A_WARPS_SMALL
+#define MOEQ_A_WARPS_SMALL 4
 #endif
 #ifndef MOEQ_A_RPW
 #define MOEQ_A_RPW 2
@@ -247,7 +252,11 @@ __device__ __forceinline__ uint32_t row_abs_max(const uint4 *src, int64_t K, int
     return __reduce_max_sync(0xFFFFFFFFu, m);
 }
 
-__global__ void __launch_bounds__(MOEQ_A_WARPS * 32, MOEQ_A_MINB) amax_kernel(const uint16_t *__restrict__ in,
+// NW warps per CTA; the register bound follows from NW and MINB (large
+// inputs: 85 registers for 3 resident 8-warp CTAs; small: 4-warp CTAs
+// without a tighter bound than 3 per SM)
+template <int NW, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) amax_kernel(const uint16_t *__restrict__ in,
                                                    int64_t stride, int64_t K, GroupArgs g,
                                                    Gather gt,
                                                    uint32_t *__restrict__ amax_bits,
@@ -1104,11 +1113,16 @@ cudaError_t launch_amax_scale(const void *in, int64_t stride, int64_t K, const G
     cudaError_t e = launch_pdl(zero_words_kernel, eblocks, 256, 0, s, bits, (int)g.num_experts);
     if (e != cudaSuccess) return e;
     if (g.total_rows > 0) {
-        // enough warps to fill the GPU on small inputs, 4 rows each on large
-        const int rows_per_warp = g.total_rows >= 65536 ? MOEQ_A_RPW : 1;
+        // one row per warp in small CTAs on small inputs (more, shorter CTAs
+        // to fill the GPU), MOEQ_A_RPW rows per warp on large ones
+        const bool large = g.total_rows >= 65536;
+        const int rows_per_warp = large ? MOEQ_A_RPW : 1;
+        const int cta_warps = large ? MOEQ_A_WARPS : MOEQ_A_WARPS_SMALL;
         int64_t warps = (g.total_rows + rows_per_warp - 1) / rows_per_warp;
-        int64_t blocks = (warps + MOEQ_A_WARPS - 1) / MOEQ_A_WARPS;
-        e = launch_pdl(amax_kernel, (unsigned)blocks, MOEQ_A_WARPS * 32, 0, s,
+        int64_t blocks = (warps + cta_warps - 1) / cta_warps;
+        auto kern = large ? amax_kernel<MOEQ_A_WARPS, MOEQ_A_MINB>
+                          : amax_kernel<MOEQ_A_WARPS_SMALL, MOEQ_A_MINB>;
+        e = launch_pdl(kern, (unsigned)blocks, cta_warps * 32, 0, s,
                        reinterpret_cast<const uint16_t *>(in), stride, K, g, gt, bits, err,
                        rows_per_warp);
         if (e != cudaSuccess) return e;
