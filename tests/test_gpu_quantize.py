@@ -194,6 +194,30 @@ def test_amax_scale_full_size():
     assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
 
+@pytest.mark.parametrize("T", [65535, 65539])
+def test_amax_scale_launch_shapes(T):
+    """Both launch shapes of the amax pass: below 65536 rows one row per warp
+    in 4-warp CTAs (65535: the last CTA has 3 warps), from 65536 rows two
+    rows per warp in 8-warp CTAs (65539: the last warp has one row); the
+    largest value of each expert lies in its group's last rows."""
+    need_gpu()
+    K, E = 128, 5
+    counts = [T // 4, 0, T // 4, T - 3 * (T // 4) - 7, T // 4 + 7]
+    ids = np.array([3, 1, 0, 4, 2], np.int32)
+    ro, ids = groups_from_counts(counts, ids)
+    assert int(ro[-1]) == T
+    x = synth.bf16_normal((T, K), 1.0, seed=5)
+    for g in range(len(counts)):
+        if counts[g]:
+            x[int(ro[g + 1]) - 1, (17 * g) % K] = -300.0 - g   # tail row of the group
+    out = torch.full((E,), -1.0, device=DEV)
+    moeq.grouped_amax_scale(x.to(DEV), to_dev_u32(ro), to_dev_i32(ids), out, E)
+    want = _oracle_ts(x.float().numpy(), ro, ids, E)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    # expert 1 has no rows (scale 1); expert 3's amax is its group's tail value 300
+    assert want[1] == 1.0 and want[3] == np.float32(300.0) / np.float32(2688.0)
+
+
 def test_padded_scale_offsets():
     need_gpu()
     rng = np.random.default_rng(4)
