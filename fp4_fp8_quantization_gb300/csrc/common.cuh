@@ -340,6 +340,23 @@ __device__ __forceinline__ float silu_lookup(uint32_t gb, const float *tab) {
     return mag < (kSiluE0 << 7) ? __fmul_rn(g, 0.5f) : __fmul_rn(g, g >= 0.0f ? 1.0f : 0.0f);
 }
 
+// silu_lookup with the table at shared-memory address tab, read by an
+// explicit shared load (issued only for gates inside the band): the same
+// entries and closed forms.
+__device__ __forceinline__ float silu_lookup_shared(uint32_t gb, uint32_t tab) {
+    const uint32_t mag = gb & 0x7FFFu;
+    const uint32_t t = mag - (kSiluE0 << 7);
+    const float g = __uint_as_float(gb << 16);
+    if (t < kSiluHalf) {
+        float v;
+        asm volatile("ld.shared.f32 %0, [%1];"
+                     : "=f"(v)
+                     : "r"(tab + 4u * (t + ((gb & 0x8000u) ? kSiluHalf : 0u))));
+        return v;
+    }
+    return mag < (kSiluE0 << 7) ? __fmul_rn(g, 0.5f) : __fmul_rn(g, g >= 0.0f ? 1.0f : 0.0f);
+}
+
 // h = silu(g) * u for two (gate, up) words (gate bits in the low half, up
 // in the high half), silu by table.
 __device__ __forceinline__ F2 swiglu2_tab(uint32_t w0, uint32_t w1, const float *tab) {

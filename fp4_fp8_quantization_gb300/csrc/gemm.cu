@@ -60,8 +60,12 @@ enum Kind { kFp8Rowwise = 0, kNvfp4 = 1, kMxfp8 = 2, kMxfp4 = 3 };
 // mainloop's element format (MXFP4 -> E2M1, MXFP8 -> E4M3, E8M0 scales).
 enum Epi { kBf16 = 0, kSwiglu = 1, kSwigluMx = 2 };
 
+// Groups a launch with the SiLU table may hold (its tile prefix shares the
+// CTA's shared memory with the table).
+constexpr int kSiluMaxGroups = 512;
+
 template <int KIND, int EPI, int BN_, int STAGES_, int ACC_BUFS_, int EPI_WARPS_, int SF_WARPS_,
-          int PAIR_, int SF_LOADER_ = 1>
+          int PAIR_, int SF_LOADER_ = 1, int SILU_TAB_ = 0>
 struct Cfg {
     static constexpr int BM = 128;                              // rows of A per CTA
     static constexpr int PAIR = PAIR_;                          // CTAs per MMA (cta_group)
@@ -100,12 +104,23 @@ struct Cfg {
     static constexpr int SF_WARP0 = 2 + SF_LOADER;
     static constexpr int EPI_WARP0 = SF_WARP0 + SF_WARPS;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-    // fused SwiGLU epilogues on CTA pairs: the control warpgroup (producer,
-    // MMA and scale-copy warps) gives registers to the epilogue warpgroups,
-    // whose SiLU evaluations otherwise spill (setmaxnreg acts per warpgroup
-    // and redistributes exactly the registers the block is launched with;
-    // the host checks the compiled count before launching)
-    static constexpr bool NREG = EPI != kBf16 && PAIR_ == 2 && EPI_WARP0 == 4 && THREADS == 384;
+    // SwiGLU epilogues: silu(gate) from a table of every bf16 gate in the
+    // band where it has no closed form (32 KB, after the stages), where it
+    // fits beside a tile prefix of kSiluMaxGroups groups; else computed
+    static constexpr bool SILU_TAB =
+        SILU_TAB_ && EPI != kBf16 &&
+        STAGES * STAGE_BYTES + (int)kSiluTableBytes + 1024 + 4 * (kSiluMaxGroups + 1) + 512 <=
+            227 * 1024;
+    static constexpr int SILU_BYTES = SILU_TAB ? (int)kSiluTableBytes : 0;
+    static constexpr int MAXG = SILU_TAB ? kSiluMaxGroups : kMaxGroups;  // groups per launch
+    // fused SwiGLU epilogues on CTA pairs that compute the SiLU: the control
+    // warpgroup (producer, MMA and scale-copy warps) gives registers to the
+    // epilogue warpgroups, whose SiLU evaluations otherwise spill (setmaxnreg
+    // acts per warpgroup and redistributes exactly the registers the block is
+    // launched with; the host checks the compiled count before launching).
+    // With the table the kernel fits its launch registers as it is.
+    static constexpr bool NREG =
+        EPI != kBf16 && !SILU_TAB && PAIR_ == 2 && EPI_WARP0 == 4 && THREADS == 384;
     static constexpr int LAUNCH_REGS = 65536 / THREADS / 8 * 8;
     static constexpr int NREG_CTRL = 104;
     static constexpr int NREG_EPI =
@@ -122,13 +137,15 @@ struct Cfg {
     static constexpr bool EPI_BUF_FITS =
         STAGES * STAGE_BYTES + EPI_WARPS * 2048 + 1024 <= 222 * 1024;
     static constexpr int EPI_BUF_BYTES = (EPI == kBf16 && EPI_BUF_FITS) ? 2048 : 0;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + 1024;
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + SILU_BYTES + 1024;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(!NREG || (NREG_EPI >= LAUNCH_REGS && NREG_EPI <= 256 &&
                             32 * EPI_WARP0 * NREG_CTRL + 32 * EPI_WARPS * NREG_EPI <=
                                 THREADS * LAUNCH_REGS),
                   "register split by warpgroups");
-    static_assert(SMEM_BYTES <= 222 * 1024, "dynamic shared memory beside the static part");
+    // dynamic part + the tile prefix + the barriers and flags (under 512 bytes)
+    static_assert(SMEM_BYTES + 4 * (MAXG + 1) + 512 <= 227 * 1024, "shared memory per CTA");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale atoms");
@@ -253,12 +270,27 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
 //             E4M3 scale code, writes the 8 packed bytes.  gate and up are
 //             bf16((acc * s) * rsr): s the expert scale, rsr the row scale
 //             (1 without row scales, an exact no-op).
+// h = silu(gate) * up for two (gate, up) pairs of bf16 values held in fp32
+// (gates in the low halves of q0, q1, ups in the high halves): silu from
+// the table at shared-memory address stab, which holds exactly the computed
+// values and reduces to the same closed forms outside its band, or computed.
+template <bool TAB>
+__device__ __forceinline__ F2 swiglu_pairs(F2 q0, F2 q1, uint32_t stab) {
+    if constexpr (TAB)
+        return mul2(f2(silu_lookup_shared(__float_as_uint(f2_lo(q0)) >> 16, stab),
+                       silu_lookup_shared(__float_as_uint(f2_lo(q1)) >> 16, stab)),
+                    f2(f2_hi(q0), f2_hi(q1)));
+    else
+        return swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
+}
+
 template <class C, int KIND, int EPI>
 __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32_t (&r)[32],
                                                    int nc, int e, int64_t row, bool valid,
                                                    float rs, float inv_out, float rsr = 1.0f,
                                                    uint32_t sbuf = 0, int nvalid = 0,
-                                                   const CUtensorMap *tmc = nullptr) {
+                                                   const CUtensorMap *tmc = nullptr,
+                                                   uint32_t stab = 0) {
     if (EPI == kBf16) {
         const int lane = threadIdx.x & 31;
         uint32_t w[16];
@@ -348,7 +380,7 @@ __device__ __forceinline__ uint32_t epilogue_chunk(const Params &p, const uint32
                 mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2), rr2));
             const F2 q1 = round_bf16_2(mul2(
                 mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2), rr2));
-            const F2 hh = swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
+            const F2 hh = swiglu_pairs<C::SILU_TAB>(q0, q1, stab);
             h[i] = f2_lo(hh);
             h[i + 1] = f2_hi(hh);
         }
@@ -426,10 +458,11 @@ __device__ __forceinline__ void copy_stage_scales(uint32_t tmem, const uint8_t *
 // (gate, up = bf16(acc * s)), then the MX rule of the quantizer on the fp32
 // h (scale code from the block amax, elements = elem(h * 2^(127 - c))).
 // Writes 32 (E4M3) or 16 (packed E2M1) bytes; returns the E8M0 code.
-template <int KIND>
+template <int KIND, bool TAB>
 __device__ __forceinline__ uint32_t epilogue_mx_block(const Params &p, const uint32_t (&r0)[32],
                                                       const uint32_t (&r1)[32], int nc,
-                                                      int64_t row, bool valid, float rs) {
+                                                      int64_t row, bool valid, float rs,
+                                                      uint32_t stab) {
     float h[32];
     const F2 rs2 = f2(rs, rs);
 #pragma unroll
@@ -441,7 +474,7 @@ __device__ __forceinline__ uint32_t epilogue_mx_block(const Params &p, const uin
                 mul2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), rs2));
             const F2 q1 = round_bf16_2(
                 mul2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), rs2));
-            const F2 hh = swiglu2(f2_lo(q0), f2_lo(q1), f2_hi(q0), f2_hi(q1));
+            const F2 hh = swiglu_pairs<TAB>(q0, q1, stab);
             h[half * 16 + i] = f2_lo(hh);
             h[half * 16 + i + 1] = f2_hi(hh);
         }
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ uint64_t sf_drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ uint32_t prefix[kMaxGroups + 1];
+    __shared__ uint32_t prefix[C::MAXG + 1];
     // stages each loading warp of this CTA went through (announced on the
     // barrier, copies issued), stored once when it stops; read by the even
     // CTA at teardown
@@ -558,6 +591,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         prefix[0] = 0;
         fence_barrier_init();
     }
+    // the SiLU table, after the stages (visible after the barrier below)
+    constexpr int kSiluOff = C::STAGES * C::STAGE_BYTES + C::EPI_WARPS * C::EPI_BUF_BYTES;
+    if constexpr (C::SILU_TAB) build_silu_table(reinterpret_cast<float *>(smem + kSiluOff));
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -826,6 +862,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             else
                 mbar_arrive_cluster_relaxed(tempty0 + 8u * buf);
         };
+        const uint32_t silu_tab = smem_u32(smem + kSiluOff);
         // this warp's bf16 staging buffer, after the stages
         const uint32_t sbuf = smem_u32(smem + C::STAGES * C::STAGE_BYTES) +
                               (uint32_t)(warp - C::EPI_WARP0) * C::EPI_BUF_BYTES;
@@ -883,8 +920,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int64_t prow = (int64_t)__ldg(p.a_sf_offsets + tl.g) + lrow;
 #pragma unroll
                     for (int b2 = 0; b2 < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W) / 2; ++b2) {
-                        const uint32_t code = epilogue_mx_block<KIND>(
-                            p, r[2 * b2], r[2 * b2 + 1], ncol0 + b2 * 64, row, valid, rs);
+                        const uint32_t code = epilogue_mx_block<KIND, C::SILU_TAB>(
+                            p, r[2 * b2], r[2 * b2 + 1], ncol0 + b2 * 64, row, valid, rs,
+                            silu_tab);
                         if (mb_in_group) store_sf_byte_mx(p, prow, ncol0 + b2 * 64, valid ? code : 0u);
                     }
                 } else {
@@ -892,7 +930,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int ch = 0; ch < (C::CHUNKS_W > 4 ? 4 : C::CHUNKS_W); ++ch)
                         sfbytes |= epilogue_chunk<C, KIND, EPI>(p, r[ch], ncol0 + ch * 32, e, row,
                                                                 valid, rs, inv_out, rsr, sbuf,
-                                                                nvalid, &tmC)
+                                                                nvalid, &tmC, silu_tab)
                                    << (8 * ch);
                 }
             } else {
@@ -1068,9 +1106,12 @@ int sm_count() {
 }
 
 template <int KIND, int EPI, int BN, int STAGES, int ACC_BUFS, int EPI_WARPS, int SF_WARPS = 1,
-          int PAIR = 1>
+          int PAIR = 1, int SILU_TAB = 0>
 cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
-    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, PAIR, MOEQ_SF_LOADER>;
+    using C = Cfg<KIND, EPI, BN, STAGES, ACC_BUFS, EPI_WARPS, SF_WARPS, PAIR, MOEQ_SF_LOADER,
+                  SILU_TAB>;
+    // the kernel's tile prefix holds at most C::MAXG groups
+    if (a.groups.num_groups > C::MAXG) return cudaErrorInvalidValue;
     const int64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? a.K / 2 : a.K;
     const int64_t T = a.groups.total_rows;
     const int64_t E = a.groups.num_experts;
@@ -1255,6 +1296,11 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 #ifndef MOEQ_MX8_STAGES
 #define MOEQ_MX8_STAGES 6
 #endif
+// Fused SwiGLU epilogues of the FP4 kinds take silu(gate) from a
+// shared-memory table (1) or compute it (0).
+#ifndef MOEQ_SILU_TAB
+#define MOEQ_SILU_TAB 1
+#endif
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     constexpr int P = MOEQ_FP4_PAIR;
@@ -1270,12 +1316,19 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     if (a.kind == kNvfp4 && a.epi == kBf16)
         return run_gemm<kNvfp4, kBf16, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS, MOEQ_FP4_EPI_WARPS,
                         MOEQ_SF_WARPS, P>(a, s);
+    // fused SwiGLU on FP4: silu by table up to kSiluMaxGroups groups, computed
+    // beyond (the same bytes either way)
+    const bool tab = a.groups.num_groups <= kSiluMaxGroups;
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
-        return run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
+        return tab ? run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                              MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P, MOEQ_SILU_TAB>(a, s)
+                   : run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                              MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp4 && a.epi == kSwigluMx)
-        return run_gemm<kMxfp4, kSwigluMx, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
-                        MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
+        return tab ? run_gemm<kMxfp4, kSwigluMx, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                              MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P, MOEQ_SILU_TAB>(a, s)
+                   : run_gemm<kMxfp4, kSwigluMx, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
+                              MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp8 && a.epi == kSwigluMx)
         return run_gemm<kMxfp8, kSwigluMx, 128, MOEQ_MX8_STAGES, 2, 8>(a, s);
     if (a.kind == kMxfp4 && a.epi == kBf16)

@@ -5,7 +5,9 @@ against the CPU oracle through the C ABI:
 * the grouped GEMMs at the scheduler's maximum of 1024 groups (most of them
   empty or 1-8 rows, expert ids repeating), FP8 rowwise and NVFP4;
 * a long reduction (K = 16384) in the block-scaled GEMM;
-* the fused SwiGLU kernel at 1024 groups, byte-identical to the chained path."""
+* the fused SwiGLU kernels (NVFP4 and MXFP4) byte-identical to the chained
+  path at 512 groups (silu from the kernel's shared-memory table) and at 513
+  and 1024 groups (silu computed: the table's launches hold at most 512)."""
 import numpy as np
 import pytest
 import torch
@@ -101,23 +103,34 @@ def test_nvfp4_blockscaled_max_groups_and_long_k(G, K):
     assert np.all(c[~written] == np.float32(CANARY).view(np.uint32) >> 16)
 
 
-def test_fused_swiglu_max_groups_equals_chained():
+@pytest.mark.parametrize("fmt,G", [("nvfp4", 512), ("nvfp4", 513), ("nvfp4", 1024),
+                                   ("mxfp4", 512), ("mxfp4", 513)])
+def test_fused_swiglu_many_groups_equals_chained(fmt, G):
     need_gpu()
-    G, E, I, K = 1024, 96, 128, 256
+    E, I, K = 96, 128, 256
     ro, ids = _many_groups(G, E, seed=10)
     so = Q.padded_scale_offsets(ro)
     T, rows = int(ro[-1]) + 2, int(so[-1]) + 128
-    a, asf, b, bsf, es = blockscaled_inputs("nvfp4", T, E, 2 * I, K, rows, seed=11, device=DEV)
-    ots = synth.uniform((E,), 0.05, 0.2, seed=12, device=DEV)
+    a, asf, b, bsf, es = blockscaled_inputs(fmt, T, E, 2 * I, K, rows, seed=11, device=DEV)
     ro_d, so_d, ids_d = to_dev_u32(ro), to_dev_u32(so), to_dev_i32(ids)
     y = torch.zeros((T, 2 * I), dtype=torch.bfloat16, device=DEV)
-    moeq.grouped_matmul_blockscaled("nvfp4", y, a, asf, b, bsf, es, ro_d, so_d, ids_d, 2 * I, K,
+    moeq.grouped_matmul_blockscaled(fmt, y, a, asf, b, bsf, es, ro_d, so_d, ids_d, 2 * I, K,
                                     rows)
-    c1 = torch.full((T, I // 2), 0xA5, dtype=torch.uint8, device=DEV)
-    s1 = torch.full((moeq.sf_bytes(rows, I // 16),), 0x5A, dtype=torch.uint8, device=DEV)
-    moeq.swiglu_quantize(c1, s1, y, ots, ro_d, so_d, ids_d, E, rows)
-    c2, s2 = torch.full_like(c1, 0xA5), torch.full_like(s1, 0x5A)
-    moeq.grouped_matmul_swiglu(c2, s2, a, asf, b, bsf, es, ots, ro_d, so_d, ids_d, I, K, rows)
+    if fmt == "nvfp4":
+        ots = synth.uniform((E,), 0.05, 0.2, seed=12, device=DEV)
+        c1 = torch.full((T, I // 2), 0xA5, dtype=torch.uint8, device=DEV)
+        s1 = torch.full((moeq.sf_bytes(rows, I // 16),), 0x5A, dtype=torch.uint8, device=DEV)
+        moeq.swiglu_quantize(c1, s1, y, ots, ro_d, so_d, ids_d, E, rows)
+        c2, s2 = torch.full_like(c1, 0xA5), torch.full_like(s1, 0x5A)
+        moeq.grouped_matmul_swiglu(c2, s2, a, asf, b, bsf, es, ots, ro_d, so_d, ids_d, I, K, rows)
+    else:
+        c1 = torch.full((T, I // 2), 0xA5, dtype=torch.uint8, device=DEV)
+        s1 = torch.full((moeq.sf_bytes(rows, I // 32),), 0x5A, dtype=torch.uint8, device=DEV)
+        moeq.swiglu_quantize_mx(fmt, c1, s1, y, ro_d, so_d, ids_d, E, rows)
+        c2, s2 = torch.full_like(c1, 0xA5), torch.full_like(s1, 0x5A)
+        moeq.grouped_matmul_swiglu_mx(fmt, c2, s2, a, asf, b, bsf, es, ro_d, so_d, ids_d, I, K,
+                                      rows)
     torch.cuda.synchronize()
     assert torch.equal(c1, c2) and torch.equal(s1, s2)
+    assert (c1[:int(ro[-1])] != 0).float().mean() > 0.3
     assert moeq.get_device_error() == 0
