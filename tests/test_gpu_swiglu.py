@@ -149,6 +149,40 @@ def test_fused_equals_chained_small(I, K):
     assert (c1[:int(ro[-1])] != 0).float().mean() > 0.3
 
 
+@pytest.mark.parametrize("empty_groups", [0, 507])
+def test_fused_equals_chained_extreme_scales(empty_groups):
+    """Expert scales that push the bf16 gates below the SiLU table's band
+    (1e-36: subnormal and tiny gates), into it (1), above it (1e4: |g| >=
+    128) and past the bf16 range (1e38: +-inf gates, NaN from -inf * 0), and
+    zero: the fused kernel's table lookups and closed forms give the chained
+    kernel's bytes."""
+    need_gpu()
+    I, K = 128, 256
+    # 507 empty groups appended make 513: a launch past the table kernel's
+    # 512 groups, which computes the SiLU
+    counts = [130, 7, 129, 64, 1, 200] + [0] * empty_groups
+    ids = np.array([0, 1, 2, 3, 4, 5] + [g % 6 for g in range(empty_groups)], np.int32)
+    ro, ids = groups_from_counts(counts, ids)
+    so = Q.padded_scale_offsets(ro)
+    rows = int(so[-1])
+    T = int(ro[-1])
+    a, asf, b, bsf, _ = blockscaled_inputs("nvfp4", T, 6, 2 * I, K, rows, seed=41)
+    es = torch.tensor([1e-36, 1.0, 1e4, 1e38, 0.0, 3e-8], dtype=torch.float32)
+    ots = torch.tensor([1.0, 0.1, 1e3, 1.0, 1.0, 1e-6], dtype=torch.float32)
+    c1, s1, c2, s2 = _fused_and_chained(a, asf, b, bsf, es, ots, ro, so, ids, I, K, rows)
+    assert torch.equal(c1, c2)
+    assert torch.equal(s1, s2)
+    # the cases occurred: infinite gates, gates below the band, gates above it
+    y = torch.zeros((T, 2 * I), dtype=torch.bfloat16, device=DEV)
+    moeq.grouped_matmul_blockscaled("nvfp4", y, a.to(DEV), asf.to(DEV), b.to(DEV), bsf.to(DEV),
+                                    es.to(DEV), to_dev_u32(ro), to_dev_u32(so), to_dev_i32(ids),
+                                    2 * I, K, rows)
+    g = y[:, 0::2].float().cpu()
+    assert torch.isinf(g).any() and (g == float("-inf")).any()
+    assert ((g != 0) & (g.abs() < 2.0 ** -25)).any()
+    assert (g.abs() >= 128).any() and torch.isfinite(g[(g.abs() >= 128)]).any()
+
+
 def test_fused_equals_chained_full_size():
     """128 experts, 131072 rows, K = 4096, I = 1536: whole buffers equal."""
     need_gpu()

@@ -121,6 +121,28 @@ def test_fused_mx_equals_chained(fmt, I, K, with_es):
     assert moeq.get_device_error() == 0
 
 
+@pytest.mark.parametrize("empty_groups", [0, 507])
+def test_fused_mx_equals_chained_extreme_scales(empty_groups):
+    """MXFP4 with expert scales that put the bf16 gates below, inside, above
+    and past the range of the SiLU table (and zero): the fused kernel's
+    table lookups and closed forms give the chained kernel's bytes."""
+    need_gpu()
+    I, K = 128, 256
+    # 507 empty groups appended make 513: a launch past the table kernel's
+    # 512 groups, which computes the SiLU
+    counts = [130, 7, 129, 64, 1, 200] + [0] * empty_groups
+    ids = np.array([0, 1, 2, 3, 4, 5] + [g % 6 for g in range(empty_groups)], np.int32)
+    ro, ids = groups_from_counts(counts, ids)
+    so = Q.padded_scale_offsets(ro)
+    rows = int(so[-1])
+    a, asf, b, bsf, _ = blockscaled_inputs("mxfp4", int(ro[-1]), 6, 2 * I, K, rows, seed=43)
+    es = torch.tensor([1e-36, 1.0, 1e4, 1e38, 0.0, 3e-8], dtype=torch.float32)
+    c1, s1, c2, s2 = _fused_and_chained_mx("mxfp4", a, asf, b, bsf, es, ro, so, ids, I, K, rows)
+    assert torch.equal(c1, c2)
+    assert torch.equal(s1, s2)
+    assert moeq.get_device_error() == 0
+
+
 def test_fused_mx_full_size():
     """128 experts, 16384 tokens top-8 (131072 rows), K = 4096, I = 1536, MXFP4
     throughout: whole buffers equal to the chained path."""
