@@ -113,16 +113,19 @@ struct Cfg {
             227 * 1024;
     static constexpr int SILU_BYTES = SILU_TAB ? (int)kSiluTableBytes : 0;
     static constexpr int MAXG = SILU_TAB ? kSiluMaxGroups : kMaxGroups;  // groups per launch
-    // fused SwiGLU epilogues on CTA pairs that compute the SiLU: the control
-    // warpgroup (producer, MMA and scale-copy warps) gives registers to the
-    // epilogue warpgroups, whose SiLU evaluations otherwise spill (setmaxnreg
-    // acts per warpgroup and redistributes exactly the registers the block is
-    // launched with; the host checks the compiled count before launching).
-    // With the table the kernel fits its launch registers as it is.
-    static constexpr bool NREG =
-        EPI != kBf16 && !SILU_TAB && PAIR_ == 2 && EPI_WARP0 == 4 && THREADS == 384;
+    // fused SwiGLU epilogues on CTA pairs: the control warpgroups (producer,
+    // MMA and scale-copy warps) give registers to the two epilogue
+    // warpgroups (setmaxnreg acts per warpgroup and redistributes exactly the
+    // registers the block is launched with; the host checks the compiled
+    // count before launching).  Computing the SiLU (384 threads): control
+    // 104, epilogue 200, without which the MX epilogue spills.  The table
+    // kernels fit their 168 launch registers with 2 scale-copy warps; with 6
+    // (512 threads, 128 at launch) the two control warpgroups keep 96 and the
+    // epilogue gets 160.
     static constexpr int LAUNCH_REGS = 65536 / THREADS / 8 * 8;
-    static constexpr int NREG_CTRL = 104;
+    static constexpr bool NREG = EPI != kBf16 && PAIR_ == 2 && EPI_WARP0 % 4 == 0 &&
+                                 EPI_WARPS == 8 && (SILU_TAB ? THREADS == 512 : THREADS == 384);
+    static constexpr int NREG_CTRL = SILU_TAB ? 96 : 104;
     static constexpr int NREG_EPI =
         NREG ? (THREADS * LAUNCH_REGS - 32 * EPI_WARP0 * NREG_CTRL) / (32 * EPI_WARPS) / 8 * 8 : 0;
     static constexpr int ACC_COLS = BN;
@@ -1268,9 +1271,16 @@ cudaError_t run_gemm(const GemmArgs &a, cudaStream_t s) {
 // Warps issuing the shared -> TMEM scale copies (atoms dealt round-robin).
 // Two, with the scale loads in the producer warp, is measured fastest on the
 // 128-expert NVFP4 workload (fused 0.86 ms vs 1.00 ms with one copy warp and
-// a scale-load warp; 3, 4 or 6 copy warps 1.07-1.09 ms).
+// a scale-load warp; 3, 4 or 6 copy warps 1.07-1.09 ms, in earlier builds).
 #ifndef MOEQ_SF_WARPS
 #define MOEQ_SF_WARPS 2
+#endif
+// The fused NVFP4 kernel with the SiLU table (12 scale atoms per stage):
+// six copy warps, 0.644-0.649 against 0.659-0.660 ms with two on the
+// 128-expert workload; the MXFP4 one (6 atoms per stage) keeps two (0.634
+// against 0.608 ms with six).
+#ifndef MOEQ_SF_WARPS_NVFP4_TAB
+#define MOEQ_SF_WARPS_NVFP4_TAB 6
 #endif
 // CTA-pair tiles (M = 256 over two SMs, tcgen05 cta_group::2, each SM
 // staging half of the B tile) for the FP4 kinds: 0.78 vs 0.81 ms fused and
@@ -1321,7 +1331,9 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     const bool tab = a.groups.num_groups <= kSiluMaxGroups;
     if (a.kind == kNvfp4 && a.epi == kSwiglu)
         return tab ? run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
-                              MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P, MOEQ_SILU_TAB>(a, s)
+                              MOEQ_SWIGLU_EPI_WARPS,
+                              MOEQ_SILU_TAB && P == 2 ? MOEQ_SF_WARPS_NVFP4_TAB : MOEQ_SF_WARPS, P,
+                              MOEQ_SILU_TAB>(a, s)
                    : run_gemm<kNvfp4, kSwiglu, MOEQ_FP4_BN, FP4_ST, MOEQ_FP4_ACC_BUFS,
                               MOEQ_SWIGLU_EPI_WARPS, MOEQ_SF_WARPS, P>(a, s);
     if (a.kind == kMxfp4 && a.epi == kSwigluMx)
